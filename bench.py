@@ -1,0 +1,324 @@
+#!/usr/bin/env python
+"""Throughput of one GMM EM step on a B300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload embed_10m]
+
+A step is one EM iteration over the whole data set: parameter preparation,
+the fused logit / log-sum-exp / statistics kernel, the fixed-order reduction
+and the M-step.  The default workload is the 10M x 128 x 1024 diagonal model
+on bf16 embedding-like data (inputs larger than L2, so no flush is needed).
+With --gpus N > 1 (launched by torchrun) every rank runs an independent
+replica; nothing is exchanged on the data path, only the timing maximum.
+
+--impl reference times the float64 CPU oracle on a bounded prefix of the
+same workload per step and scales it to the full N (EM cost is linear in N).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "EM iter/s and N·K·D/s at N=10M,D=128,K=1024 diag; % tensor-core peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    def __init__(self, dev_index: int):
+        self.dev = dev_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{dev_index}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, x: float) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_rows_for(w, seconds: float, X_host_prefix, init, probe_rows=1000):
+    """Rows of the workload the oracle handles in about `seconds`."""
+    import oracle
+    probe = min(probe_rows, X_host_prefix.shape[0])
+    t0 = time.perf_counter()
+    oracle.em_step(X_host_prefix[:probe], *init, w.cov)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    return int(max(probe, min(X_host_prefix.shape[0], probe * seconds / dt)))
+
+
+def cpu_oracle_step(w, X_host, init, rows):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.em_step(X_host[:rows], *init, w.cov)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, w, ws, rank):
+    """The float64 CPU oracle as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    cap = min(w.N, 400_000)
+    X = W.make_data(w, cap, device=dev)
+    init = W.make_init(w, X)
+    Xh = X.float().cpu().numpy()
+    rows = oracle_rows_for(w, args.ref_step_seconds, Xh, init)
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        cpu_oracle_step(w, Xh, init, min(rows, 1000))
+    times = [cpu_oracle_step(w, Xh, init, rows) for _ in range(args.steps)]
+    per_full = statistics.mean(times) * (w.N / rows)
+    value = 1.0 / per_full
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "EM iter/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_full * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, "oracle"),
+        "cpu_baseline": {"value": value, "unit": "EM iter/s", "cores": oracle.threads(),
+                         "kind": "oracle",
+                         "sample": f"1 EM step on the first {rows} rows per step, scaled by N/{rows}"},
+        "e2e": {"value": value, "unit": "EM iter/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, precision):
+    return {"workload": w.name, "N": w.N, "D": w.D, "K": w.K, "cov": w.cov, "x_dtype": w.x_dtype,
+            "precision": precision, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (no flush)" if w.N * w.D * (2 if w.x_dtype == "bf16" else 4) > 126e6
+            else "L2 flushed between steps"}
+
+
+def run_ours(args, w, ws, rank, local):
+    import em_gmm_step_02_b300 as G
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    X = W.make_data(w, device=dev)
+    lw0, mu0, var0 = W.make_init(w, X)
+    p = [torch.tensor(a, device=dev) for a in (lw0, mu0, var0)]
+    x_bytes = X.numel() * X.element_size()
+    flush = None
+    if x_bytes <= 126e6:
+        flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+    opts = G.gmm_default_opts(precision=args.precision)
+    G.gmm_reserve(w.N, w.D, w.K, w.cov, w.x_dtype, precision=args.precision)
+
+    def step():
+        if flush is not None:
+            flush.add_(1.0)
+        return G.gmm_em_step(X, *p, w.cov, out=p, opts=opts)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert G.gmm_stream_status() == 0, G.gmm_last_error()
+
+    stream = torch.cuda.current_stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    launches = 0
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        G.gmm_profile_begin()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+            launches += G.gmm_last_launch_count()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        main_ms, main_launches = G.gmm_profile_end()
+    barrier(ws)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ws, ms)
+    status = G.gmm_stream_status()
+    assert status == 0, G.gmm_last_error()
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+        Xh.copy_(X)
+        ph = [a.cpu().pin_memory() for a in p]
+        outh = [torch.empty_like(a).pin_memory() for a in ph]
+        llh = torch.empty(1, dtype=torch.float64).pin_memory()
+        Xd = torch.empty_like(X)
+        pd = [torch.empty_like(a) for a in p]
+        h2d = Xh.numel() * Xh.element_size() + sum(a.numel() * a.element_size() for a in ph)
+        d2h = sum(a.numel() * a.element_size() for a in outh) + 8
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            Xd.copy_(Xh, non_blocking=True)
+            for d_, h_ in zip(pd, ph):
+                d_.copy_(h_, non_blocking=True)
+            *o, ll = G.gmm_em_step(Xd, *pd, w.cov, out=pd, opts=opts)
+            for h_, d_ in zip(outh, o):
+                h_.copy_(d_, non_blocking=True)
+            llh.copy_(ll, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(ws, e0.elapsed_time(e1) / args.steps)
+        e2e = {"value": ws * 1e3 / e2e_ms, "unit": "EM iter/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+        del Xh, Xd
+
+    if rank != 0:
+        return
+    peaks, peaks_kind = load_peaks()
+    flops = 8.0 * w.N * w.K * w.D
+    per_launch_ms = main_ms / max(1, main_launches)
+    launches_per_step = max(1, main_launches // args.steps)
+    achieved = flops / launches_per_step / (per_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": METRIC, "value": ws * 1e3 / ms_max, "unit": "EM iter/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic", "config": config_of(w, args.precision),
+        "nkd_per_s": ws * w.N * w.K * w.D * 1e3 / ms_max,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "fused_em_kernel", "launch_ms": per_launch_ms,
+                     "peak_source": f"{peaks_kind} bf16 burst (fp16 has the same nominal rate)",
+                     "work": "8*N*K*D MMA flops per step"},
+        "hbm": {"x_bytes_per_step": x_bytes, "gbs": x_bytes / (ms_max * 1e-3) / 1e9,
+                "peak_gbs": float(peaks["hbm_gbs"])},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu and ws == 1:
+        import oracle
+        cap = min(w.N, 400_000)
+        Xh = X[:cap].float().cpu().numpy()
+        init = (lw0, mu0, var0)
+        rows = oracle_rows_for(w, args.cpu_seconds, Xh, init)
+        t = cpu_oracle_step(w, Xh, init, rows)
+        line["cpu_baseline"] = {"value": 1.0 / (t * w.N / rows), "unit": "EM iter/s",
+                                "cores": oracle.threads(), "kind": "oracle",
+                                "sample": f"1 EM step on the first {rows} rows, scaled by N/{rows}"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="embed_10m", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--precision", default="auto", choices=["auto", "fast", "precise"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=8.0)
+    args = ap.parse_args()
+    w = W.WORKLOADS[args.workload]
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, w, ws, rank)
+    else:
+        run_ours(args, w, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,542 @@
+// gmm_api.cu -- host side of the C ABI declared in include/gmm.h: argument
+// checks, the launch plan (precision, cluster size, single or two-pass),
+// the per-device workspace, and the launch sequence of one EM step.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "gmm.h"
+#include "gmm_kernels.cuh"
+#include "layout.cuh"
+
+using namespace gmm;
+
+namespace {
+
+thread_local std::string g_error;
+thread_local int32_t g_launches = 0;
+
+// Optional timing of the main (fused) kernel launches: an event pair around
+// each, read back by gmm_profile_end().
+thread_local bool g_prof_on = false;
+thread_local std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_prof_events;
+thread_local int32_t g_prof_launches = 0;
+
+int fail(int code, const std::string& msg) {
+  g_error = msg;
+  return code;
+}
+
+#define CUDA_TRY(expr)                                                                  \
+  do {                                                                                  \
+    cudaError_t e_ = (expr);                                                            \
+    if (e_ != cudaSuccess) return fail(GMM_ERR_CUDA, std::string(#expr) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------------ plan
+struct Plan {
+  int64_t N;
+  int D, K, cov_diag, x_bf16;
+  bool fast;
+  int nch, np, nst;
+  int K_pad, n_slices;
+  int n_tiles;
+  bool two_pass;
+  int C;              // cluster size of the single pass / of pass 1
+  int n_kgroups;      // pass 1 K groups (two-pass)
+  int tg;             // tile groups of the statistics pass
+  int tg1;            // tile groups of pass 1 (two-pass)
+  int F;
+  int flush;
+  size_t smem;
+  // workspace offsets
+  size_t off_meta, off_pimg, off_cadj, off_iscale, off_part, off_llpart, off_lsepart, off_lse, off_ll;
+  size_t n_llpart;
+  size_t ws_bytes;
+};
+
+constexpr int kCombineBlocks = 296;
+constexpr size_t kStatusBytes = 256;
+
+int device_sms() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  return sms;
+}
+
+}  // namespace
+
+namespace {
+
+template <int NP, int NCH, int NST>
+constexpr size_t cfg_smem() {
+  return Cfg<NP, NCH, NST>::kOffSmall + sizeof(Small) + 1024;   // + base alignment slack
+}
+
+size_t fused_smem(int np, int nch, int nst) {
+  size_t b = 0;
+  if (np == 1 && nch == 1 && nst == 2) b = cfg_smem<1, 1, 2>();
+  else if (np == 1 && nch == 2 && nst == 2) b = cfg_smem<1, 2, 2>();
+  else if (np == 2 && nch == 1 && nst == 1) b = cfg_smem<2, 1, 1>();
+  return std::max<size_t>(b, 120 * 1024);   // one CTA per SM: it owns all of tensor memory
+}
+
+const void* fused_fn(int np, int nch, int nst) {
+  if (np == 1 && nch == 1 && nst == 2) return kernel_handle(K_FUSED_1_1_2);
+  if (np == 1 && nch == 2 && nst == 2) return kernel_handle(K_FUSED_1_2_2);
+  if (np == 2 && nch == 1 && nst == 1) return kernel_handle(K_FUSED_2_1_1);
+  return nullptr;
+}
+
+// Largest number of C-CTA clusters of the fused kernel resident at once.
+int max_clusters(const void* fn, size_t smem, int C) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_pair(fn, C);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int sms = device_sms();
+  int n = std::max(1, sms / C);
+  if (C > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C * n, 1, 1);
+    cfg.blockDim = dim3(416, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int got = 0;
+    if (cudaOccupancyMaxActiveClusters(&got, fn, &cfg) == cudaSuccess && got > 0) n = got;
+    else cudaGetLastError();
+  }
+  cache[key] = n;
+  return n;
+}
+
+int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t cov, int32_t dtype,
+              const gmm_opts& o, bool need_device) {
+  if (N < 1) return fail(GMM_ERR_INVALID_ARG, "N must be >= 1");
+  if (D < 1) return fail(GMM_ERR_INVALID_ARG, "D must be >= 1");
+  if (K < 1) return fail(GMM_ERR_INVALID_ARG, "K must be >= 1");
+  if (cov != GMM_SPHERICAL && cov != GMM_DIAG) return fail(GMM_ERR_INVALID_ARG, "cov_type must be 0 or 1");
+  if (dtype != GMM_F32 && dtype != GMM_BF16) return fail(GMM_ERR_INVALID_ARG, "x_dtype must be 0 or 1");
+  if (o.precision < GMM_PREC_AUTO || o.precision > GMM_PREC_PRECISE)
+    return fail(GMM_ERR_INVALID_ARG, "unknown precision");
+  if (!(o.reg_covar >= 0.f) || !(o.var_floor >= 0.f) || !std::isfinite(o.reg_covar) || !std::isfinite(o.var_floor))
+    return fail(GMM_ERR_INVALID_ARG, "reg_covar and var_floor must be finite and >= 0");
+  if (!(o.x_absmax >= 0.f) || !std::isfinite(o.x_absmax)) return fail(GMM_ERR_INVALID_ARG, "x_absmax must be finite and >= 0");
+  if (D > kMaxD) return fail(GMM_ERR_UNSUPPORTED, "D > 128 is not supported");
+  if (K > 8192) return fail(GMM_ERR_UNSUPPORTED, "K > 8192 is not supported");
+  if (N > (int64_t(1) << 40)) return fail(GMM_ERR_UNSUPPORTED, "N too large");
+  if (X && (reinterpret_cast<uintptr_t>(X) & 15)) return fail(GMM_ERR_INVALID_ARG, "X must be 16-byte aligned");
+  p.N = N; p.D = D; p.K = K; p.cov_diag = cov == GMM_DIAG; p.x_bf16 = dtype == GMM_BF16;
+  const int prec = o.precision == GMM_PREC_AUTO ? (p.x_bf16 ? GMM_PREC_FAST : GMM_PREC_PRECISE) : o.precision;
+  p.fast = prec == GMM_PREC_FAST;
+  p.nch = D <= 64 ? 1 : 2;
+  p.np = p.fast ? 1 : 2;
+  p.nst = p.fast ? 2 : 1;
+  if (!p.fast && p.nch != 1) return fail(GMM_ERR_UNSUPPORTED, "PRECISE arithmetic supports D <= 64");
+  p.n_slices = (K + kSlice - 1) / kSlice;
+  p.two_pass = p.n_slices > 8;
+  if (p.two_pass) p.n_slices = (p.n_slices + 7) / 8 * 8;   // whole 8-slice groups for pass 1
+  p.K_pad = p.n_slices * kSlice;
+  p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
+  p.smem = fused_smem(p.np, p.nch, p.nst);
+  p.F = 2 * p.nch * kAtomElems + 1;
+  p.flush = p.fast ? 64 : 16;
+  const int sms = need_device ? device_sms() : 148;
+  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  if (!p.two_pass) {
+    p.C = p.n_slices;
+    p.n_kgroups = 1;
+    int mc = need_device ? max_clusters(fn, p.smem, p.C) : std::max(1, sms / p.C);
+    p.tg = std::max(1, std::min(p.n_tiles, mc));
+    p.tg1 = 0;
+  } else {
+    p.C = 8;
+    p.n_kgroups = (p.n_slices + 7) / 8;
+    int mc = need_device ? max_clusters(fn, p.smem, 8) : std::max(1, sms / 8);
+    p.tg1 = std::max(1, std::min(p.n_tiles, mc / p.n_kgroups));
+    p.tg = std::max(1, std::min(p.n_tiles, sms / p.n_slices));
+  }
+  // workspace layout
+  size_t off = kStatusBytes;
+  p.off_meta = off; off += align256(sizeof(Meta));
+  p.off_ll = off; off += 256;
+  const size_t piece = static_cast<size_t>(2 * p.nch) * kChunkBytes;
+  p.off_pimg = off; off += align256(static_cast<size_t>(p.n_slices) * p.np * piece);
+  p.off_cadj = off; off += align256(sizeof(float) * p.K_pad);
+  p.off_iscale = off; off += align256(sizeof(float) * p.K_pad);
+  p.off_part = off; off += align256(sizeof(double) * static_cast<size_t>(p.tg) * p.K_pad * p.F);
+  p.n_llpart = std::max<size_t>(p.tg, kCombineBlocks);
+  p.off_llpart = off; off += align256(sizeof(double) * p.n_llpart);
+  p.off_lsepart = off;
+  p.off_lse = off;
+  if (p.two_pass) {
+    off += align256(sizeof(float) * static_cast<size_t>(p.n_kgroups) * N);
+    p.off_lse = off;
+    off += align256(sizeof(float) * static_cast<size_t>(N));
+  }
+  p.ws_bytes = off;
+  return GMM_OK;
+}
+
+// ------------------------------------------------------------------ workspace
+struct Workspace {
+  uint8_t* buf = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<int, Workspace> g_ws;
+
+int get_workspace(size_t need, uint8_t** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  Workspace& w = g_ws[dev];
+  if (w.bytes < need) {
+    uint32_t old_status = 0;
+    if (w.buf) {
+      CUDA_TRY(cudaDeviceSynchronize());
+      CUDA_TRY(cudaMemcpy(&old_status, w.buf, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+      CUDA_TRY(cudaFree(w.buf));
+      w.buf = nullptr;
+      w.bytes = 0;
+    }
+    size_t bytes = std::max(need, w.bytes + w.bytes / 2);
+    CUDA_TRY(cudaMalloc(&w.buf, bytes));
+    CUDA_TRY(cudaMemset(w.buf, 0, kStatusBytes));
+    if (old_status) CUDA_TRY(cudaMemcpy(w.buf, &old_status, sizeof(uint32_t), cudaMemcpyHostToDevice));
+    w.bytes = bytes;
+  }
+  *out = w.buf;
+  return GMM_OK;
+}
+
+int status_to_code(uint32_t st) {
+  if (st & ST_TIMEOUT) return fail(GMM_ERR_TIMEOUT, "a device-side wait exceeded its bound");
+  if (st & ST_NONFINITE) return fail(GMM_ERR_NONFINITE, "a parameter is not finite or a variance is not positive");
+  if (st & ST_RANGE) return fail(GMM_ERR_RANGE, "data magnitude outside the FAST operand range");
+  return GMM_OK;
+}
+
+template <typename... Args>
+int launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (cluster > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* argv[] = {static_cast<void*>(&args)...};
+  CUDA_TRY(cudaLaunchKernelExC(&cfg, fn, argv));
+  ++g_launches;
+  return GMM_OK;
+}
+
+// Launch of a main kernel, bracketed by events when profiling is on.
+template <typename... Args>
+int launch_main(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster, Args... args) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (g_prof_on) {
+    CUDA_TRY(cudaEventCreate(&e0));
+    CUDA_TRY(cudaEventCreate(&e1));
+    CUDA_TRY(cudaEventRecord(e0, s));
+  }
+  int r = launch(fn, grid, block, smem, s, cluster, args...);
+  if (r) return r;
+  if (g_prof_on) {
+    CUDA_TRY(cudaEventRecord(e1, s));
+    g_prof_events.emplace_back(e0, e1);
+    ++g_prof_launches;
+  }
+  return GMM_OK;
+}
+
+int set_smem_attr(const void* fn, size_t smem) {
+  CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+  return GMM_OK;
+}
+
+int check_ptr(const void* p, const char* name) {
+  if (!p) return fail(GMM_ERR_INVALID_ARG, std::string(name) + " is NULL");
+  if (reinterpret_cast<uintptr_t>(p) & 3) return fail(GMM_ERR_INVALID_ARG, std::string(name) + " is not 4-byte aligned");
+  return GMM_OK;
+}
+
+// prep: scan (optional), meta, parameter images
+int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, const float* var,
+             const gmm_opts& o, uint8_t* ws, cudaStream_t s) {
+  Meta* meta = reinterpret_cast<Meta*>(ws + p.off_meta);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  if (o.x_absmax <= 0.f) {
+    CUDA_TRY(cudaMemsetAsync(&meta->absmax_bits, 0, sizeof(uint32_t), s));
+    const int64_t n_elems = p.N * p.D;
+    const int64_t per_vec = p.x_bf16 ? 8 : 4;
+    const int sms = device_sms();
+    if (n_elems % per_vec == 0) {
+      const int64_t n_vec = n_elems / per_vec;
+      int blocks = static_cast<int>(std::min<int64_t>(4 * sms, (n_vec + 255) / 256));
+      int r = launch(kernel_handle(K_ABSMAX_VEC), dim3(blocks), dim3(256), 0, s, 1,
+                     static_cast<const uint4*>(X), n_vec, p.x_bf16, meta);
+      if (r) return r;
+    } else {
+      int blocks = static_cast<int>(std::min<int64_t>(4 * sms, (n_elems + 255) / 256));
+      int r = launch(kernel_handle(K_ABSMAX), dim3(blocks), dim3(256), 0, s, 1, X, n_elems,
+                     p.x_bf16, meta);
+      if (r) return r;
+    }
+  }
+  {
+    // bf16 data in FAST stay unshifted: they are then exact in fp16
+    int use_shift = (p.fast && p.x_bf16) ? 0 : 1;
+    float hint = o.x_absmax;
+    int r = launch(kernel_handle(K_META), dim3(1), dim3(128), 0, s, 1, mu, p.D, p.K, use_shift,
+                   hint, meta, status);
+    if (r) return r;
+  }
+  {
+    const void* fn = kernel_handle(p.fast ? K_PARAMS_FAST : K_PARAMS_PRECISE);
+    int r = launch(fn, dim3(p.K_pad), dim3(128), 0, s, 1, lw, mu, var, p.D, p.K, p.cov_diag, p.nch,
+                   static_cast<const Meta*>(meta), ws + p.off_pimg, reinterpret_cast<float*>(ws + p.off_cadj),
+                   reinterpret_cast<float*>(ws + p.off_iscale), status);
+    if (r) return r;
+  }
+  return GMM_OK;
+}
+
+FusedArgs base_args(const Plan& p, const void* X, uint8_t* ws) {
+  FusedArgs a = {};
+  a.X = X;
+  a.N = p.N;
+  a.D = p.D;
+  a.K = p.K;
+  a.K_pad = p.K_pad;
+  a.x_bf16 = p.x_bf16;
+  a.n_tiles = p.n_tiles;
+  a.flush_tiles = p.flush;
+  a.F = p.F;
+  a.p_img = ws + p.off_pimg;
+  a.cadj = reinterpret_cast<const float*>(ws + p.off_cadj);
+  a.iscale = reinterpret_cast<const float*>(ws + p.off_iscale);
+  a.meta = reinterpret_cast<const Meta*>(ws + p.off_meta);
+  a.part = reinterpret_cast<double*>(ws + p.off_part);
+  a.ll_part = reinterpret_cast<double*>(ws + p.off_llpart);
+  a.lse_part = reinterpret_cast<float*>(ws + p.off_lsepart);
+  a.lse_in = reinterpret_cast<const float*>(ws + p.off_lse);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  return a;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+extern "C" {
+
+void gmm_default_opts(gmm_opts* o) {
+  if (!o) return;
+  o->precision = GMM_PREC_AUTO;
+  o->reg_covar = 1e-6f;
+  o->var_floor = 0.f;
+  o->x_absmax = 0.f;
+  o->loglik_on_host = 0;
+}
+
+const char* gmm_last_error(void) { return g_error.c_str(); }
+
+int32_t gmm_last_launch_count(void) { return g_launches; }
+
+size_t gmm_workspace_bytes(int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
+                           const gmm_opts* opts) {
+  gmm_opts o;
+  gmm_default_opts(&o);
+  if (opts) o = *opts;
+  Plan p;
+  int dev_count = 0;
+  bool have_dev = cudaGetDeviceCount(&dev_count) == cudaSuccess && dev_count > 0;
+  if (!have_dev) cudaGetLastError();
+  if (make_plan(p, nullptr, N, D, K, cov_type, x_dtype, o, have_dev) != GMM_OK) return 0;
+  return p.ws_bytes;
+}
+
+int gmm_reserve(int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype, const gmm_opts* opts) {
+  gmm_opts o;
+  gmm_default_opts(&o);
+  if (opts) o = *opts;
+  Plan p;
+  int r = make_plan(p, nullptr, N, D, K, cov_type, x_dtype, o, true);
+  if (r) return r;
+  uint8_t* ws = nullptr;
+  return get_workspace(p.ws_bytes, &ws);
+}
+
+int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
+                const float* log_weights, const float* means, const float* vars, float* new_log_weights,
+                float* new_means, float* new_vars, double* total_loglik, const gmm_opts* opts, void* stream) {
+  g_launches = 0;
+  gmm_opts o;
+  gmm_default_opts(&o);
+  if (opts) o = *opts;
+  if (!X) return fail(GMM_ERR_INVALID_ARG, "X is NULL");
+  int r;
+  if ((r = check_ptr(log_weights, "log_weights")) || (r = check_ptr(means, "means")) ||
+      (r = check_ptr(vars, "vars")) || (r = check_ptr(new_log_weights, "new_log_weights")) ||
+      (r = check_ptr(new_means, "new_means")) || (r = check_ptr(new_vars, "new_vars")))
+    return r;
+  if (!total_loglik) return fail(GMM_ERR_INVALID_ARG, "total_loglik is NULL");
+  Plan p;
+  if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = nullptr;
+  if ((r = get_workspace(p.ws_bytes, &ws))) return r;
+  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  if ((r = set_smem_attr(fn, p.smem))) return r;
+
+  if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
+  CUDA_TRY(cudaMemsetAsync(ws + p.off_part, 0, sizeof(double) * static_cast<size_t>(p.tg) * p.K_pad * p.F, s));
+
+  FusedArgs a = base_args(p, X, ws);
+  int n_ll = p.tg;
+  if (!p.two_pass) {
+    a.mode = MODE_EM;
+    a.C = p.C;
+    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), p.smem, s, p.C, a))) return r;
+  } else {
+    // pass 1: per-point normaliser over each group of 1024 components
+    FusedArgs a1 = a;
+    a1.mode = MODE_LSE;
+    a1.C = 8;
+    if ((r = launch_main(fn, dim3(8 * p.tg1, p.n_kgroups), dim3(416), p.smem, s, 8, a1))) return r;
+    float* lse = reinterpret_cast<float*>(ws + p.off_lse);
+    if ((r = launch(kernel_handle(K_LSE_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
+                    static_cast<const float*>(a.lse_part), p.n_kgroups, p.N, lse,
+                    reinterpret_cast<double*>(ws + p.off_llpart))))
+      return r;
+    n_ll = kCombineBlocks;
+    // pass 2: statistics of every slice given the normaliser
+    FusedArgs a2 = a;
+    a2.mode = MODE_GIVEN;
+    a2.C = 1;
+    a2.ll_part = nullptr;
+    if ((r = launch_main(fn, dim3(p.n_slices, p.tg), dim3(416), p.smem, s, 1, a2))) return r;
+  }
+  double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
+  {
+    float reg = o.reg_covar, floor_ = o.var_floor;
+    int Dp = p.nch * kAtomElems;
+    if ((r = launch(kernel_handle(K_FINALIZE), dim3(p.K), dim3(128), 0, s, 1,
+                    static_cast<const double*>(a.part), p.tg, p.K_pad, p.F, Dp, p.D, p.K, p.N, p.cov_diag, reg,
+                    floor_, 32768.0, static_cast<const Meta*>(a.meta), reinterpret_cast<const double*>(ws + p.off_llpart),
+                    n_ll, new_log_weights, new_means, new_vars, means, vars, ll_dev)))
+      return r;
+  }
+  if (o.loglik_on_host) {
+    CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    uint32_t st = 0;
+    CUDA_TRY(cudaMemcpy(&st, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    if (st) {
+      CUDA_TRY(cudaMemset(ws, 0, sizeof(uint32_t)));
+      return status_to_code(st);
+    }
+  }
+  return GMM_OK;
+}
+
+int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
+                     const float* log_weights, const float* means, const float* vars, int32_t m, float* resp_out,
+                     int32_t* idx_out, double* total_loglik, const gmm_opts* opts, void* stream) {
+  (void)X; (void)N; (void)D; (void)K; (void)cov_type; (void)x_dtype; (void)log_weights; (void)means;
+  (void)vars; (void)m; (void)resp_out; (void)idx_out; (void)total_loglik; (void)opts; (void)stream;
+  return fail(GMM_ERR_UNSUPPORTED, "gmm_predict_topm is not available yet");
+}
+
+int gmm_stream_status(void* stream) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  uint8_t* buf = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    auto it = g_ws.find(dev);
+    if (it == g_ws.end() || !it->second.buf) return GMM_OK;
+    buf = it->second.buf;
+  }
+  uint32_t st = 0;
+  CUDA_TRY(cudaMemcpy(&st, buf, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  if (st) CUDA_TRY(cudaMemset(buf, 0, sizeof(uint32_t)));
+  return status_to_code(st);
+}
+
+void gmm_profile_begin(void) {
+  for (auto& e : g_prof_events) {
+    cudaEventDestroy(e.first);
+    cudaEventDestroy(e.second);
+  }
+  g_prof_events.clear();
+  g_prof_launches = 0;
+  g_prof_on = true;
+}
+
+int gmm_profile_end(double* main_kernel_ms, int32_t* launches) {
+  g_prof_on = false;
+  double tot = 0.0;
+  int rc = GMM_OK;
+  for (auto& e : g_prof_events) {
+    float ms = 0.f;
+    if (rc == GMM_OK) {
+      cudaError_t err = cudaEventSynchronize(e.second);
+      if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, e.first, e.second);
+      if (err != cudaSuccess) rc = fail(GMM_ERR_CUDA, std::string("profile events: ") + cudaGetErrorString(err));
+    }
+    tot += ms;
+    cudaEventDestroy(e.first);
+    cudaEventDestroy(e.second);
+  }
+  g_prof_events.clear();
+  if (main_kernel_ms) *main_kernel_ms = tot;
+  if (launches) *launches = g_prof_launches;
+  g_prof_launches = 0;
+  return rc;
+}
+
+void gmm_release(void) {
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  for (auto& kv : g_ws) {
+    if (kv.second.buf) {
+      int cur = 0;
+      cudaGetDevice(&cur);
+      cudaSetDevice(kv.first);
+      cudaDeviceSynchronize();
+      cudaFree(kv.second.buf);
+      cudaSetDevice(cur);
+    }
+  }
+  g_ws.clear();
+}
+
+}  // extern "C"

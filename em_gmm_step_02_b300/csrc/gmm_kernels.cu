@@ -1,0 +1,804 @@
+// gmm_kernels.cu -- the EM-step kernels for sm_103a.
+//
+// Method: "Flash-GMM: A Memory-Efficient Kernel for Scalable Soft Clustering",
+// section 2 (E-step responsibilities through a log-sum-exp over K weighted
+// Gaussian terms; M-step from responsibility-weighted sufficient statistics)
+// and section 3 (a naive GPU EM stores and re-reads the N x K responsibility
+// matrix; here it lives only in on-chip tiles).
+//
+// Data path of one EM step (diagonal covariance; spherical uses the same
+// path with the variance repeated over the D dimensions):
+//   prep     per component: operand image of [mu/s2, -1/(2 s2)] (scaled to
+//            log2 units) and the constant c_k = log pi_k - 1/2 sum log(2 pi s2)
+//            - 1/2 sum mu^2/s2.
+//   fused    per 128-point tile, per 128-component slice (one CTA each, the
+//            slices of one tile forming a thread-block cluster):
+//              logits   l = [x, x^2] . [mu/s2, -1/(2 s2)]^T + c     (tcgen05, TMEM)
+//              softmax  row max / sum in registers, slices combined through
+//                       distributed shared memory, r = 2^(l - lse)
+//              stats    [S1 | S2 | S0] += R^T [x | x^2 | 1]           (tcgen05, TMEM)
+//            statistics leave tensor memory every few tiles into fp64
+//            per-cluster partials; nothing of size N x K is ever stored.
+//   finalize fixed-order fp64 reduction of the partials and the M-step.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "gmm_kernels.cuh"
+#include "layout.cuh"
+#include "ptx.cuh"
+
+namespace gmm {
+
+constexpr double kLog2e = 1.4426950408889634073599246810019;
+constexpr double kLn2 = 0.69314718055994530941723212145818;
+constexpr double kLog2Pi = 1.8378770664093454835606594728112;  // ln(2 pi)
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool cond) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r) : "r"(static_cast<uint32_t>(cond)), "r"(id), "r"(nthreads) : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ============================================================== scan of |X|
+__global__ void absmax_kernel(const void* __restrict__ X, int64_t n_elems, int x_bf16,
+                              Meta* __restrict__ meta) {
+  float m = 0.f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  if (x_bf16) {
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(X);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_elems; i += stride)
+      m = fmaxf(m, fabsf(__bfloat162float(x[i])));
+  } else {
+    const float* x = static_cast<const float*>(X);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_elems; i += stride)
+      m = fmaxf(m, fabsf(x[i]));
+  }
+  // NaN propagates as a huge bound (caught later as a range error).
+  if (m != m) m = CUDART_INF_F;
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(&meta->absmax_bits, __float_as_uint(m));
+}
+
+// Vectorised scan for 16-byte aligned data (8 bf16 or 4 f32 per load).
+__global__ void absmax_vec_kernel(const uint4* __restrict__ X, int64_t n_vec, int x_bf16,
+                                  Meta* __restrict__ meta) {
+  float m = 0.f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
+    uint4 v = __ldg(X + i);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (x_bf16) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = fmaxf(m, fabsf(__uint_as_float(w[j])));
+    }
+  }
+  if (m != m) m = CUDART_INF_F;
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(&meta->absmax_bits, __float_as_uint(m));
+}
+
+// ============================================================== meta
+// shift = mean of the component means (per dimension; zero when use_shift is
+// 0, which keeps bf16 data exact in fp16); scale = power of two that keeps
+// |x'| <= 127, so that x'^2 and its fp16 pieces stay inside the fp16 range.
+__global__ void meta_kernel(const float* __restrict__ means, int D, int K, int use_shift, float absmax_hint,
+                            Meta* __restrict__ meta, uint32_t* __restrict__ status) {
+  __shared__ float red[kMaxD];
+  const int d = threadIdx.x;
+  float sh = 0.f;
+  if (d < D && use_shift) {
+    double s = 0.0;
+    for (int k = 0; k < K; ++k) s += static_cast<double>(means[static_cast<int64_t>(k) * D + d]);
+    sh = static_cast<float>(s / K);
+    if (!isfinite(sh)) {
+      atomicOr(status, ST_NONFINITE);
+      sh = 0.f;
+    }
+  }
+  if (d < kMaxD) meta->shift[d] = sh;
+  red[d] = fabsf(sh);
+  __syncthreads();
+  if (d == 0) {
+    float bmax = 0.f;
+    for (int i = 0; i < D; ++i) bmax = fmaxf(bmax, red[i]);
+    const float xa = absmax_hint > 0.f ? absmax_hint : __uint_as_float(meta->absmax_bits);
+    float bound = xa + bmax;
+    float scale = 1.f;
+    if (!(bound < 1e30f)) {
+      atomicOr(status, ST_RANGE);
+      bound = 1.f;
+    }
+    if (bound > 0.f) {
+      int e = static_cast<int>(floorf(log2f(127.f / bound)));
+      e = max(-100, min(100, e));
+      scale = ldexpf(1.f, e);
+      if (bound * scale > 127.5f) scale *= 0.5f;   // guard against rounding at the boundary
+    }
+    meta->scale = scale;
+    meta->inv_scale = 1.f / scale;
+  }
+}
+
+// ============================================================== params
+// One block per (padded) component.  Builds that component's rows of the
+// per-slice parameter operand images (fp16; PRECISE adds a second image
+// holding the rounding remainder, so that hi + lo carries 22 bits):
+//   columns [0, D)        mu'/s2' * log2(e)        (x-part)
+//   columns [Dp, Dp + D)  -1/(2 s2') * log2(e)     (x^2-part)
+// in the same swizzled K-major layout as the data tiles, and the logit
+// constant in log2 units.  x' = (x - shift) * scale, s2' = s2 * scale^2.
+template <bool kFast>
+__global__ void params_kernel(const float* __restrict__ log_weights, const float* __restrict__ means,
+                              const float* __restrict__ vars, int D, int K, int cov_diag, int nch,
+                              const Meta* __restrict__ meta, uint8_t* __restrict__ p_img,
+                              float* __restrict__ cadj, float* __restrict__ iscale,
+                              uint32_t* __restrict__ status) {
+  const int k = blockIdx.x;
+  const int d = threadIdx.x;   // blockDim.x == 128
+  const int Dp = nch * kAtomElems;
+  __shared__ double red_c[128];
+  __shared__ float red_m[128];
+  const bool valid_k = k < K;
+  double b1 = 0.0, b2 = 0.0, cpart = 0.0;
+  bool bad = false;
+  if (valid_k && d < D) {
+    const float mu = means[static_cast<int64_t>(k) * D + d];
+    const float v = cov_diag ? vars[static_cast<int64_t>(k) * D + d] : vars[k];
+    bad = !isfinite(mu) || !isfinite(v) || !(v > 0.f);
+    const double sc = meta->scale;
+    const double mup = (static_cast<double>(mu) - meta->shift[d]) * sc;
+    const double vp = static_cast<double>(v) * sc * sc;
+    b1 = mup / vp * kLog2e;
+    b2 = -0.5 / vp * kLog2e;
+    cpart = log(static_cast<double>(v)) + kLog2Pi + mup * mup / vp;
+  }
+  if (bad) atomicOr(status, ST_NONFINITE);
+  red_c[d] = cpart;
+  red_m[d] = static_cast<float>(fmax(fabs(b1), fabs(b2)));
+  __syncthreads();
+  for (int o = 64; o > 0; o >>= 1) {
+    if (d < o) {
+      red_c[d] += red_c[d + o];
+      red_m[d] = fmaxf(red_m[d], red_m[d + o]);
+    }
+    __syncthreads();
+  }
+  // per-component scale keeping the fp16 operands in range
+  float s = 1.f;
+  if (red_m[0] > 0.f) {
+    int e = static_cast<int>(floorf(log2f(16384.f / red_m[0])));
+    s = ldexpf(1.f, max(-120, min(120, e)));
+  }
+  if (d == 0) {
+    float lw = valid_k ? log_weights[k] : -CUDART_INF_F;
+    if (valid_k && (lw != lw || lw == CUDART_INF_F)) atomicOr(status, ST_NONFINITE);
+    float c = -CUDART_INF_F;
+    if (valid_k && lw > -CUDART_INF_F) c = static_cast<float>((static_cast<double>(lw) - 0.5 * red_c[0]) * kLog2e);
+    cadj[k] = c;
+    iscale[k] = valid_k ? 1.f / s : 0.f;
+  }
+  // write this component's row of the operand images (thread d owns column d)
+  const int slice = k / kSlice, row = k % kSlice;
+  const int np = kFast ? 1 : 2;
+  const size_t piece_bytes = static_cast<size_t>(2 * nch) * kChunkBytes;
+  uint8_t* img = p_img + static_cast<size_t>(slice) * np * piece_bytes;
+  if (d < Dp) {
+    for (int part = 0; part < 2; ++part) {
+      const double val = (valid_k && d < D) ? (part == 0 ? b1 : b2) : 0.0;
+      const int c = part * nch + d / kAtomElems;
+      const uint32_t off = c * kChunkBytes + sw128_off(row, (d % kAtomElems) / 8) + (d % 8) * 2;
+      const float f = static_cast<float>(val * s);
+      const __half hi = __float2half_rn(f);
+      *reinterpret_cast<__half*>(img + off) = hi;
+      if (!kFast) *reinterpret_cast<__half*>(img + piece_bytes + off) = __float2half_rn(f - __half2float(hi));
+    }
+  }
+}
+
+// ============================================================== fused kernel
+template <int NP, int NCH, int NST>
+__global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
+  using CF = Cfg<NP, NCH, NST>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Small* S = reinterpret_cast<Small*>(sm + CF::kOffSmall);
+  volatile uint32_t* abort_flag = &S->abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const bool given = a.mode == MODE_GIVEN;
+  const bool stats = a.mode == MODE_EM || a.mode == MODE_GIVEN;
+  const int C = a.C;
+
+  // ---- which slice / which tiles
+  int rank, slice, tgroup, n_tgroups;
+  if (given) {
+    rank = 0;
+    slice = blockIdx.x;
+    tgroup = blockIdx.y;
+    n_tgroups = gridDim.y;
+  } else {
+    rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    slice = blockIdx.y * C + rank;
+    tgroup = blockIdx.x / C;
+    n_tgroups = gridDim.x / C;
+  }
+  const int kbase = slice * kSlice;
+  const int kvalid = max(0, min(kSlice, a.K - kbase));
+  const int n1 = max(16, min(kSlice, (kvalid + 15) & ~15));         // logit MMA width
+  int my_tiles = 0;
+  if (tgroup < a.n_tiles) my_tiles = (a.n_tiles - 1 - tgroup) / n_tgroups + 1;
+
+  // ---- set-up
+  if (tid == 0) {
+    S->abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S->full_a[i], 128);
+      mbar_init(&S->empty_a[i], 1);
+      mbar_init(&S->xready[i], C);
+      mbar_init(&S->xfree[i], C);
+    }
+    mbar_init(&S->p_full, 1);
+    mbar_init(&S->acc1_full, 1);
+    mbar_init(&S->acc1_empty, 256);
+    mbar_init(&S->r_full, 128);
+    mbar_init(&S->r_empty, 1);
+    mbar_init(&S->acc2_full, 1);
+    mbar_init(&S->acc2_empty, 256);
+    mbar_init(&S->drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 12) {
+    tmem_alloc(&S->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (tid >= 128 && tid < 384) {
+    const int j = tid - 128;
+    if (j < kSlice) {
+      S->cadj[j] = a.cadj[kbase + j];
+      S->iscale[j] = a.iscale[kbase + j];
+    }
+  }
+  if (tid < 128) {
+    // the all-ones operand that turns the statistics MMA into a row count
+    const uint32_t one2 = 0x3C003C00u;   // pairs of fp16 1.0
+    uint32_t* ones = reinterpret_cast<uint32_t*>(sm + CF::kOffOnes);
+    for (int i = tid; i < 512; i += 128) ones[i] = one2;
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (C > 1 && !given) cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = S->tmem_base;
+  const uint32_t acc1 = tmem + CF::kAcc1Col;
+  const uint32_t acc2 = tmem + CF::kAcc2Col;
+
+  const uint32_t sA = smem_u32(sm + CF::kOffA);
+  const uint32_t sP = smem_u32(sm + CF::kOffP);
+  const uint32_t sR = smem_u32(sm + CF::kOffR);
+  const uint32_t sOnes = smem_u32(sm + CF::kOffOnes);
+  constexpr uint32_t kAbType = 0u;   // fp16 operands (PRECISE: hi and lo pieces)
+
+  if (warp < 4) {
+    // ================================================= transform warps
+    constexpr int UPR = 8 * NCH;                     // 8-element units per row
+    const int ch = tid % UPR;                        // fixed feature unit of this thread
+    const int d0 = ch * 8;
+    const Meta* meta = a.meta;
+    float shift[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) shift[e] = d0 + e < a.D ? meta->shift[d0 + e] : 0.f;
+    const float scale = meta->scale;
+    const bool vec = (a.D % 8) == 0;
+    int j = 0;
+    for (int t = tgroup; j < my_tiles; t += n_tgroups, ++j) {
+      if (bar_red_or(2, 128, *abort_flag != 0)) break;
+      const int s = j % NST, use = j / NST;
+      if (use > 0) mbar_wait(&S->empty_a[s], (use - 1) & 1, abort_flag, a.status);
+      uint8_t* stage = sm + CF::kOffA + s * CF::kStageBytes;
+#pragma unroll 1
+      for (int i = 0; i < 128 / (128 / UPR); ++i) {
+        const int u = tid + 128 * i;
+        const int row = u / UPR;
+        const int64_t n = static_cast<int64_t>(t) * kBN + row;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        if (n < a.N && d0 < a.D) {
+          if (a.x_bf16) {
+            const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(a.X) + n * a.D + d0;
+            if (vec) {
+              uint4 v = __ldg(reinterpret_cast<const uint4*>(xr));
+              uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                x[2 * e] = __uint_as_float(w[e] << 16);
+                x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = d0 + e < a.D ? __bfloat162float(xr[e]) : 0.f;
+            }
+          } else {
+            const float* xr = static_cast<const float*>(a.X) + n * a.D + d0;
+            if (vec) {
+              float4 v0 = __ldg(reinterpret_cast<const float4*>(xr));
+              float4 v1 = __ldg(reinterpret_cast<const float4*>(xr) + 1);
+              x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+              x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = d0 + e < a.D ? xr[e] : 0.f;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = d0 + e < a.D ? (x[e] - shift[e]) * scale : 0.f;
+        }
+        const uint32_t off = (ch / 8) * kChunkBytes + sw128_off(row, ch % 8);
+        const uint32_t off2 = off + NCH * kChunkBytes;
+        if constexpr (NP == 1) {
+          uint4 hx, hq;
+          hx.x = pack_f16x2(x[0], x[1]); hx.y = pack_f16x2(x[2], x[3]);
+          hx.z = pack_f16x2(x[4], x[5]); hx.w = pack_f16x2(x[6], x[7]);
+          hq.x = pack_f16x2(x[0] * x[0], x[1] * x[1]); hq.y = pack_f16x2(x[2] * x[2], x[3] * x[3]);
+          hq.z = pack_f16x2(x[4] * x[4], x[5] * x[5]); hq.w = pack_f16x2(x[6] * x[6], x[7] * x[7]);
+          *reinterpret_cast<uint4*>(stage + off) = hx;
+          *reinterpret_cast<uint4*>(stage + off2) = hq;
+        } else {
+          float xh[8], xl[8], qh[8], ql[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            xh[e] = __half2float(__float2half_rn(x[e]));
+            xl[e] = x[e] - xh[e];
+            const float q = x[e] * x[e];
+            qh[e] = __half2float(__float2half_rn(q));
+            ql[e] = q - qh[e];
+          }
+          uint4 v;
+          v.x = pack_f16x2(xh[0], xh[1]); v.y = pack_f16x2(xh[2], xh[3]);
+          v.z = pack_f16x2(xh[4], xh[5]); v.w = pack_f16x2(xh[6], xh[7]);
+          *reinterpret_cast<uint4*>(stage + off) = v;
+          v.x = pack_f16x2(qh[0], qh[1]); v.y = pack_f16x2(qh[2], qh[3]);
+          v.z = pack_f16x2(qh[4], qh[5]); v.w = pack_f16x2(qh[6], qh[7]);
+          *reinterpret_cast<uint4*>(stage + off2) = v;
+          v.x = pack_f16x2(xl[0], xl[1]); v.y = pack_f16x2(xl[2], xl[3]);
+          v.z = pack_f16x2(xl[4], xl[5]); v.w = pack_f16x2(xl[6], xl[7]);
+          *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off) = v;
+          v.x = pack_f16x2(ql[0], ql[1]); v.y = pack_f16x2(ql[2], ql[3]);
+          v.z = pack_f16x2(ql[4], ql[5]); v.w = pack_f16x2(ql[6], ql[7]);
+          *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off2) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&S->full_a[s]);
+    }
+  } else if (warp < 12) {
+    // ================================================= softmax warps
+    const int st = tid - 128;            // 0..255
+    const int q = warp & 3;              // TMEM lane quarter
+    const int h = (warp - 4) >> 2;       // column half
+    const int nl = 32 * q + lane;        // point row inside the tile
+    const int rho = q >> 1;              // statistics half this row belongs to
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+    double ll = 0.0;
+    int flush_idx = 0;
+    int j = 0;
+    for (int t = tgroup; j < my_tiles; t += n_tgroups, ++j) {
+      if (bar_red_or(1, 256, *abort_flag != 0)) break;
+      const int64_t n = static_cast<int64_t>(t) * kBN + nl;
+      const bool valid = n < a.N;
+      mbar_wait(&S->acc1_full, j & 1, abort_flag, a.status);
+      tc_fence_after();
+      float v[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float w[16];
+        tmem_ld16(acc1 + lane_off + 64 * h + 16 * c, w);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[16 * c + e] = w[e];
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&S->acc1_empty);
+      // logits (log2 units) and the row maximum
+      float m = -CUDART_INF_F;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        const int k = 64 * h + e;
+        const float l = k < kvalid ? fmaf(v[e], S->iscale[k], S->cadj[k]) : -CUDART_INF_F;
+        v[e] = l;
+        m = fmaxf(m, l);
+      }
+      S->pair_m[h][nl] = m;
+      named_bar_sync(1, 256);
+      m = fmaxf(S->pair_m[0][nl], S->pair_m[1][nl]);
+      float ssum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 64; ++e) {
+        const float p = m == -CUDART_INF_F ? 0.f : ex2(v[e] - m);
+        v[e] = p;
+        ssum += p;
+      }
+      S->pair_s[h][nl] = ssum;
+      named_bar_sync(1, 256);
+      ssum = S->pair_s[0][nl] + S->pair_s[1][nl];
+      const float lse_loc = ssum > 0.f ? m + lg2(ssum) : -CUDART_INF_F;
+      float lse = lse_loc;
+      if (given) {
+        lse = valid ? __ldg(a.lse_in + n) : -CUDART_INF_F;
+      } else if (C > 1) {
+        const int slot = j & 1, use = j >> 1;
+        if (h == 0) {
+          if (use > 0) mbar_wait(&S->xfree[slot], (use - 1) & 1, abort_flag, a.status);
+          S->xsend[slot][nl] = lse_loc;
+        }
+        named_bar_sync(1, 256);
+        if (st == 0) {
+          fence_acq_rel_cluster();
+          const uint32_t bar = smem_u32(&S->xready[slot]);
+          for (int r = 0; r < C; ++r) mbar_arrive_remote(mapa(bar, r));
+        }
+        mbar_wait_cluster(&S->xready[slot], use & 1, abort_flag, a.status);
+        const uint32_t src = smem_u32(&S->xsend[slot][nl]);
+        float vals[8];
+        float mx = -CUDART_INF_F;
+        for (int r = 0; r < C; ++r) {
+          vals[r] = ld_cluster_f32(mapa(src, r));
+          mx = fmaxf(mx, vals[r]);
+        }
+        float s2 = 0.f;
+        for (int r = 0; r < C; ++r) s2 += mx == -CUDART_INF_F ? 0.f : ex2(vals[r] - mx);
+        lse = s2 > 0.f ? mx + lg2(s2) : -CUDART_INF_F;
+        named_bar_sync(1, 256);
+        if (st == 0) {
+          const uint32_t bar = smem_u32(&S->xfree[slot]);
+          for (int r = 0; r < C; ++r) mbar_arrive_remote(mapa(bar, r));
+        }
+      }
+      if (a.mode == MODE_LSE) {
+        if (rank == 0 && h == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
+        continue;
+      }
+      if (a.mode == MODE_EM && rank == 0 && h == 0 && valid) ll += static_cast<double>(lse);
+      // r is stored as r * 2^15 in fp16 so that small responsibilities stay
+      // out of the fp16 subnormal range; finalize divides the statistics back.
+      const float rscale = 32768.f;
+      const float f = (valid && lse > -CUDART_INF_F && m > -CUDART_INF_F) ? ex2(m - lse) * rscale : 0.f;
+      // responsibilities of this half-row into the statistics operand
+      const int ru = 2 * j + rho;          // use index of the R buffer
+      if (ru > 0) mbar_wait(&S->r_empty, (ru - 1) & 1, abort_flag, a.status);
+      const int nr = nl - 64 * rho;        // row inside the 64-point half
+      uint8_t* rbase = sm + CF::kOffR + h * 8192;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float r8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r8[e] = v[8 * c + e] * f;
+        const uint32_t off = sw128_off(nr, c);
+        if constexpr (NP == 1) {
+          uint4 w;
+          w.x = pack_f16x2(r8[0], r8[1]); w.y = pack_f16x2(r8[2], r8[3]);
+          w.z = pack_f16x2(r8[4], r8[5]); w.w = pack_f16x2(r8[6], r8[7]);
+          *reinterpret_cast<uint4*>(rbase + off) = w;
+        } else {
+          float hi[8], lo[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            hi[e] = __half2float(__float2half_rn(r8[e]));
+            lo[e] = r8[e] - hi[e];
+          }
+          uint4 w;
+          w.x = pack_f16x2(hi[0], hi[1]); w.y = pack_f16x2(hi[2], hi[3]);
+          w.z = pack_f16x2(hi[4], hi[5]); w.w = pack_f16x2(hi[6], hi[7]);
+          *reinterpret_cast<uint4*>(rbase + off) = w;
+          w.x = pack_f16x2(lo[0], lo[1]); w.y = pack_f16x2(lo[2], lo[3]);
+          w.z = pack_f16x2(lo[4], lo[5]); w.w = pack_f16x2(lo[6], lo[7]);
+          *reinterpret_cast<uint4*>(rbase + CF::kRBytes + off) = w;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&S->r_full);
+      // statistics leave tensor memory at the end of a flush period
+      const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
+      if (flush && stats) {
+        mbar_wait(&S->acc2_full, flush_idx & 1, abort_flag, a.status);
+        tc_fence_after();
+        // lanes = components 32q + lane; h = 0: S1 and S0, h = 1: S2
+        const int kl = 32 * q + lane;
+        double* prow = a.part + (static_cast<int64_t>(tgroup) * a.K_pad + kbase + kl) * a.F;
+        const int c0 = h == 0 ? 0 : CF::kDp;
+        for (int c = 0; c < CF::kDp; c += 16) {
+          float w[16];
+          tmem_ld16(acc2 + lane_off + c0 + c, w);
+          tmem_wait_ld();
+          if (kl < kvalid) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) prow[c0 + c + e] += static_cast<double>(w[e]);
+          }
+        }
+        if (h == 0) {
+          float w[16];
+          tmem_ld16(acc2 + lane_off + 2 * CF::kDp, w);
+          tmem_wait_ld();
+          if (kl < kvalid) prow[2 * CF::kDp] += static_cast<double>(w[0]);
+        }
+        tc_fence_before();
+        mbar_arrive(&S->acc2_empty);
+        ++flush_idx;
+      }
+    }
+    // log-likelihood partial of this cluster (rank 0 only)
+    if (a.mode == MODE_EM) {
+      for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, o);
+      if (lane == 0) S->ll_red[warp - 4] = ll;
+      named_bar_sync(1, 256);
+      if (st == 0 && rank == 0) {
+        double tot = 0.0;
+        for (int i = 0; i < 8; ++i) tot += S->ll_red[i];
+        a.ll_part[tgroup] = tot * kLn2;
+      }
+    }
+  } else {
+    // ================================================= MMA warp
+    if (lane == 0) {
+      const size_t pbytes = static_cast<size_t>(NP) * CF::kPieceBytes;
+      mbar_arrive_expect_tx(&S->p_full, static_cast<uint32_t>(pbytes));
+      const uint8_t* src = a.p_img + static_cast<size_t>(slice) * pbytes;
+      for (size_t o = 0; o < pbytes; o += 16384)
+        bulk_g2s(sm + CF::kOffP + o, src + o, 16384, &S->p_full);
+      mbar_wait(&S->p_full, 0, abort_flag, a.status);
+      tc_fence_after();
+
+      const uint32_t id1 = idesc_f16(kAbType, 0, 0, 128, n1);
+      const uint32_t id2 = idesc_f16(kAbType, 1, 1, 128, 2 * CF::kDp);
+      const uint32_t id0 = idesc_f16(kAbType, 1, 1, 128, 16);
+      int flush_idx = 0;
+      bool fresh = true;   // next statistics MMA starts a new accumulation
+
+      auto issue_g1 = [&](int jj) {
+        const int s = jj % NST;
+        const uint32_t stage = sA + s * CF::kStageBytes;
+        uint32_t accf = 0;
+#pragma unroll
+        for (int pr = 0; pr < (NP == 1 ? 1 : 3); ++pr) {
+          const int pa = pr == 2 ? 1 : 0;      // data piece
+          const int pp = pr == 1 ? 1 : 0;      // parameter piece
+          for (int c = 0; c < 2 * NCH; ++c)
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sdesc_sw128(stage + pa * CF::kPieceBytes + c * kChunkBytes + 32 * kk, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sP + pp * CF::kPieceBytes + c * kChunkBytes + 32 * kk, 16, 1024);
+              mma_f16_ss(acc1, ad, bd, id1, accf);
+              accf = 1;
+            }
+        }
+        mma_commit(&S->acc1_full);
+      };
+      auto wait_a = [&](int jj) {
+        mbar_wait(&S->full_a[jj % NST], (jj / NST) & 1, abort_flag, a.status);
+        tc_fence_after();
+      };
+
+      if (my_tiles > 0) {
+        wait_a(0);
+        issue_g1(0);
+        if (!stats) mma_commit(&S->empty_a[0]);
+      }
+      for (int j = 0; j < my_tiles; ++j) {
+        if (*abort_flag) break;
+        const int s = j % NST;
+        const bool next = j + 1 < my_tiles;
+        if (NST == 2 || !stats) {
+          if (next) {
+            wait_a(j + 1);
+            mbar_wait(&S->acc1_empty, j & 1, abort_flag, a.status);
+            tc_fence_after();
+            issue_g1(j + 1);
+            if (!stats) mma_commit(&S->empty_a[(j + 1) % NST]);
+          }
+        }
+        if (stats) {
+          const uint32_t stage = sA + s * CF::kStageBytes;
+          if (fresh && flush_idx > 0) {
+            mbar_wait(&S->acc2_empty, (flush_idx - 1) & 1, abort_flag, a.status);
+            tc_fence_after();
+          }
+          for (int rho = 0; rho < 2; ++rho) {
+            mbar_wait(&S->r_full, rho, abort_flag, a.status);
+            tc_fence_after();
+#pragma unroll
+            for (int pr = 0; pr < (NP == 1 ? 1 : 3); ++pr) {
+              const int prr = pr == 2 ? 1 : 0;   // responsibility piece
+              const int pf = pr == 1 ? 1 : 0;    // data piece
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sdesc_sw128(sR + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
+                const uint64_t bd = sdesc_sw128(stage + pf * CF::kPieceBytes + rho * 8192 + 2048 * kk,
+                                                kChunkBytes, 1024);
+                mma_f16_ss(acc2, ad, bd, id2, fresh ? 0u : 1u);
+                fresh = false;
+              }
+            }
+            // S0: responsibilities against an all-ones operand
+            bool fresh0 = (rho == 0) && (j == 0 || ((j) % a.flush_tiles == 0));
+            for (int prr = 0; prr < NP; ++prr)
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sdesc_sw128(sR + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
+                const uint64_t bd = sdesc_sw128(sOnes, kChunkBytes, 1024);
+                mma_f16_ss(acc2 + 2 * CF::kDp, ad, bd, id0, fresh0 ? 0u : 1u);
+                fresh0 = false;
+              }
+            mma_commit(&S->r_empty);
+          }
+          mma_commit(&S->empty_a[s]);
+          const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
+          if (flush) {
+            mma_commit(&S->acc2_full);
+            ++flush_idx;
+            fresh = true;
+          }
+          if (NST == 1 && next) {
+            wait_a(j + 1);
+            mbar_wait(&S->acc1_empty, j & 1, abort_flag, a.status);
+            tc_fence_after();
+            issue_g1(j + 1);
+          }
+        }
+      }
+      // drain: all issued MMAs complete before tensor memory is released
+      mma_commit(&S->drain);
+      mbar_wait(&S->drain, 0, abort_flag, a.status);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (C > 1 && !given) cluster_sync();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================== combine (K > 1024)
+// lse[n] = log2 sum_g 2^(lse_part[g][n]); per-block log-likelihood partials.
+__global__ void lse_combine_kernel(const float* __restrict__ lse_part, int n_groups, int64_t N,
+                                   float* __restrict__ lse, double* __restrict__ ll_part) {
+  __shared__ double red[8];
+  double acc = 0.0;
+  for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < N;
+       n += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float mx = -CUDART_INF_F;
+    for (int g = 0; g < n_groups; ++g) mx = fmaxf(mx, lse_part[static_cast<int64_t>(g) * N + n]);
+    float s = 0.f;
+    for (int g = 0; g < n_groups; ++g)
+      s += mx == -CUDART_INF_F ? 0.f : ex2(lse_part[static_cast<int64_t>(g) * N + n] - mx);
+    const float l = s > 0.f ? mx + lg2(s) : -CUDART_INF_F;
+    lse[n] = l;
+    acc += static_cast<double>(l);
+  }
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += red[i];
+    ll_part[blockIdx.x] = t * kLn2;
+  }
+}
+
+// ============================================================== finalize (M-step)
+// One block per component; fixed-order fp64 reduction over tile groups.
+__global__ void finalize_kernel(const double* __restrict__ part, int n_parts, int K_pad, int F, int Dp,
+                                int D, int K, int64_t N, int cov_diag, float reg_covar, float var_floor,
+                                double rscale,
+                                const Meta* __restrict__ meta, const double* __restrict__ ll_part,
+                                int n_ll, float* __restrict__ out_lw, float* __restrict__ out_mu,
+                                float* __restrict__ out_var, const float* __restrict__ old_mu,
+                                const float* __restrict__ old_var, double* __restrict__ ll_out) {
+  const int k = blockIdx.x;
+  const int d = threadIdx.x;
+  __shared__ double red[128];
+  double S0 = 0.0;
+  for (int g = 0; g < n_parts; ++g) S0 += part[(static_cast<int64_t>(g) * K_pad + k) * F + 2 * Dp];
+  S0 /= rscale;   // the responsibility operand carries a power-of-two scale
+  const bool empty = !(S0 >= 1e-30);
+  const double isc = meta->inv_scale;
+  double vd = 0.0;
+  float keep_mu = 0.f, keep_var = 0.f;
+  if (d < D) {
+    keep_mu = old_mu[static_cast<int64_t>(k) * D + d];
+    keep_var = cov_diag ? old_var[static_cast<int64_t>(k) * D + d] : old_var[k];
+  }
+  __syncthreads();   // every old value is read before any output is written
+  if (d < D) {
+    double S1 = 0.0, S2 = 0.0;
+    for (int g = 0; g < n_parts; ++g) {
+      const double* row = part + (static_cast<int64_t>(g) * K_pad + k) * F;
+      S1 += row[d];
+      S2 += row[Dp + d];
+    }
+    S1 /= rscale;
+    S2 /= rscale;
+    const double m1 = S1 / S0;
+    double v = (S2 / S0 - m1 * m1) * isc * isc;
+    if (v < 0.0) v = 0.0;
+    vd = v;
+    const double mu = m1 * isc + meta->shift[d];
+    out_mu[static_cast<int64_t>(k) * D + d] = empty ? keep_mu : static_cast<float>(mu);
+    if (cov_diag) {
+      const double vv = (v > var_floor ? v : static_cast<double>(var_floor)) + reg_covar;
+      out_var[static_cast<int64_t>(k) * D + d] = empty ? keep_var : static_cast<float>(vv);
+    }
+  }
+  if (!cov_diag) {
+    red[d] = vd;
+    __syncthreads();
+    for (int o = 64; o > 0; o >>= 1) {
+      if (d < o) red[d] += red[d + o];
+      __syncthreads();
+    }
+    if (d == 0) {
+      const double v = red[0] / D;
+      const double vv = (v > var_floor ? v : static_cast<double>(var_floor)) + reg_covar;
+      out_var[k] = empty ? keep_var : static_cast<float>(vv);
+    }
+  }
+  if (d == 0) out_lw[k] = empty ? -CUDART_INF_F : static_cast<float>(log(S0 / static_cast<double>(N)));
+  if (k == 0 && d == 0 && ll_out) {
+    double t = 0.0;
+    for (int i = 0; i < n_ll; ++i) t += ll_part[i];
+    *ll_out = t;
+  }
+}
+
+// Host-side handles of the kernels (launched from gmm_api.cu).
+const void* kernel_handle(KernelId id) {
+  switch (id) {
+    case K_ABSMAX: return reinterpret_cast<const void*>(&absmax_kernel);
+    case K_ABSMAX_VEC: return reinterpret_cast<const void*>(&absmax_vec_kernel);
+    case K_META: return reinterpret_cast<const void*>(&meta_kernel);
+    case K_PARAMS_FAST: return reinterpret_cast<const void*>(&params_kernel<true>);
+    case K_PARAMS_PRECISE: return reinterpret_cast<const void*>(&params_kernel<false>);
+    case K_FUSED_1_1_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 1, 2>);
+    case K_FUSED_1_2_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 2, 2>);
+    case K_FUSED_2_1_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 1, 1>);
+    case K_LSE_COMBINE: return reinterpret_cast<const void*>(&lse_combine_kernel);
+    case K_FINALIZE: return reinterpret_cast<const void*>(&finalize_kernel);
+  }
+  return nullptr;
+}
+
+}  // namespace gmm

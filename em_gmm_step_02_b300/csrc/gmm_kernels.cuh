@@ -1,0 +1,111 @@
+// gmm_kernels.cuh -- device-side data shared by the EM-step kernels and the
+// host planner: the per-call scalars and the fused kernel's argument block.
+#pragma once
+#include <cstdint>
+
+#include "layout.cuh"
+
+namespace gmm {
+
+constexpr int kMaxD = 128;
+
+// Device status bits (or-ed into a word in global memory).
+enum : uint32_t {
+  ST_TIMEOUT = 1u,
+  ST_NONFINITE = 2u,
+  ST_RANGE = 4u,
+};
+
+// Per-call scalars computed on the device before the main pass.
+struct Meta {
+  float shift[kMaxD];     // data are used as x' = (x - shift) * scale
+  float scale;            // power of two
+  float inv_scale;
+  uint32_t absmax_bits;   // max |x| over X (float bits; written by the scan)
+};
+
+enum KernelId : int {
+  K_ABSMAX, K_ABSMAX_VEC, K_META, K_PARAMS_FAST, K_PARAMS_PRECISE,
+  K_FUSED_1_1_2, K_FUSED_1_2_2, K_FUSED_2_1_1, K_LSE_COMBINE, K_FINALIZE,
+};
+
+// Host-side handle of a kernel, for cudaLaunchKernelEx (argument order and
+// types as in gmm_kernels.cu).
+const void* kernel_handle(KernelId id);
+
+enum Mode : int {
+  MODE_EM = 0,      // logits, normaliser across the cluster, statistics
+  MODE_LSE = 1,     // logits, normaliser across the cluster, write it out
+  MODE_GIVEN = 2,   // logits, normaliser read from memory, statistics
+  MODE_TOPM = 3,    // logits, normaliser and top-m across the cluster
+};
+
+struct FusedArgs {
+  const void* X;
+  int64_t N;
+  int D;
+  int K;
+  int K_pad;           // K rounded up to the slice size
+  int x_bf16;
+  int mode;
+  int C;               // CTAs per cluster (slices sharing one point tile)
+  int n_tiles;         // ceil(N / 128)
+  int flush_tiles;     // statistics leave tensor memory every this many tiles
+  int F;               // doubles per component row of the partial statistics
+  int topm;            // m of the top-m mode
+  const uint8_t* p_img;   // parameter operand images, one per slice
+  const float* cadj;      // per-component logit constant (log2 units)
+  const float* iscale;    // per-component scale of the logit accumulator
+  const Meta* meta;
+  double* part;           // partial statistics [tile group][K_pad][F]
+  double* ll_part;        // per tile group log-likelihood partials
+  float* lse_part;        // MODE_LSE output [K group][N] (log2 units)
+  const float* lse_in;    // MODE_GIVEN input [N] (log2 units)
+  float* topm_val;        // MODE_TOPM output values [K group][N][m] (log2 logits)
+  int32_t* topm_idx;      // MODE_TOPM output indices
+  uint32_t* status;
+};
+
+// Shared-memory plan of the fused kernel for NP operand pieces (1: fp16,
+// 2: bf16 hi/lo), NCH 64-feature atom columns per data part, NST data stages.
+template <int NP, int NCH, int NST>
+struct Cfg {
+  static constexpr int kPieceBytes = 2 * NCH * kChunkBytes;          // [x | x^2] for 128 rows
+  static constexpr int kStageBytes = NP * kPieceBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffP = NST * kStageBytes;
+  static constexpr int kOffR = kOffP + NP * kPieceBytes;
+  static constexpr int kRBytes = 64 * kSlice * 2;                     // 64 points x 128 comps x 16 bit
+  static constexpr int kOffOnes = kOffR + NP * kRBytes;
+  static constexpr int kOffSmall = kOffOnes + 2048;
+  static constexpr int kDp = NCH * kAtomElems;
+  static constexpr int kF2 = 2 * kDp + 16;                            // statistics columns in TMEM
+  static constexpr uint32_t kAcc1Col = 0;
+  static constexpr uint32_t kAcc2Col = 128;
+  static constexpr int kThreads = 13 * 32;
+};
+
+struct Small {
+  float cadj[kSlice];
+  float iscale[kSlice];
+  float pair_m[2][kBN];
+  float pair_s[2][kBN];
+  float xsend[2][kBN];
+  double ll_red[8];
+  uint64_t full_a[2];
+  uint64_t empty_a[2];
+  uint64_t p_full;
+  uint64_t acc1_full;
+  uint64_t acc1_empty;
+  uint64_t r_full;
+  uint64_t r_empty;
+  uint64_t acc2_full;
+  uint64_t acc2_empty;
+  uint64_t xready[2];
+  uint64_t xfree[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+}  // namespace gmm

@@ -1,0 +1,29 @@
+// layout.cuh -- shared-memory operand layouts of the tensor-core tiles.
+//
+// Every operand tile is built from 128-byte-swizzled "atoms": 8 rows of 128
+// bytes (64 sixteen-bit elements per row); inside an atom the 16-byte chunk
+// c of row r sits at chunk position (c XOR r).  An atom column covers 64
+// elements along a row; a tile of R rows stores its atom columns one after
+// another, each R/8 atoms (R * 128 bytes) long.
+//
+//   K-major use (contraction along the row):  start advances 32 bytes per
+//     16-element step inside an atom column, stride between 8-row groups
+//     (SBO) = 1024 bytes.
+//   MN-major use (contraction across rows):   start advances 2048 bytes per
+//     16-row step, SBO = 1024 bytes, LBO = bytes of one atom column.
+#pragma once
+#include <cstdint>
+
+namespace gmm {
+
+constexpr int kBN = 128;          // points per tile (tensor-core M of the logit contraction)
+constexpr int kSlice = 128;       // components per CTA
+constexpr int kAtomElems = 64;    // 16-bit elements per swizzled row
+constexpr int kChunkBytes = 128 * 128;  // one atom column of a 128-row tile
+
+// Byte offset of the 16-byte chunk `c16` (0..7) of row `r` inside one atom column.
+__host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c16) {
+  return (r >> 3) * 1024u + (r & 7u) * 128u + ((c16 ^ (r & 7u)) << 4);
+}
+
+}  // namespace gmm

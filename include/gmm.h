@@ -1,0 +1,166 @@
+/*
+ * gmm.h -- C ABI of the B300 (sm_103a) GMM EM-step library.
+ *
+ * One call runs one Expectation-Maximization iteration of a Gaussian mixture
+ * with spherical or diagonal covariance over N points in D dimensions and K
+ * components, without ever storing the N x K responsibility matrix: memory
+ * beyond X is O(K * D) (plus O(N) floats when K > 1024, see gmm_em_step).
+ * A second call returns every point's m largest responsibilities.
+ *
+ * The method (web pages it is described on):
+ *  - "Flash-GMM: A Memory-Efficient Kernel for Scalable Soft Clustering",
+ *    section 2: mixture density, E-step responsibilities in log space
+ *    (log-sum-exp), M-step for N_k, pi_k, mu_k and the variance; section 3:
+ *    the N x K responsibility matrix is what a naive GPU EM must store and
+ *    re-read; conclusion: multi-assignment from the final responsibilities.
+ *  - "ML0094 GMM vs K-Means": EM steps, soft assignment.
+ *  - "GMMXX" README, "Covariance Coverage": parameter shapes (K,) for
+ *    spherical and (K, D) for diagonal variances.
+ *
+ * Conventions for every entry point
+ *  - X is row-major N x D, contiguous, on the device, either float32 or
+ *    bfloat16 (x_dtype).  Its base address must be 16-byte aligned.
+ *  - Parameters are float32 device arrays: log_weights (K), means (K x D
+ *    row-major), vars (K for spherical, K x D for diagonal).  Log-weights need
+ *    not be normalised; a log-weight of -inf marks a dead component.
+ *  - All array arguments are caller-owned device pointers unless stated; the
+ *    library never frees them.  Work is enqueued on `stream` (a cudaStream_t,
+ *    NULL = legacy default stream) and the call returns without waiting,
+ *    unless opts->loglik_on_host is set.
+ *  - The library keeps one internal workspace per device (O(K * D) bytes
+ *    times the number of SMs, plus O(N) floats when K > 1024).  It is grown
+ *    on demand with cudaMalloc, so a call that needs a bigger workspace
+ *    synchronises the device first; gmm_workspace_bytes() reports the size
+ *    and gmm_reserve() allocates it up front.  Calls on different streams of
+ *    one device must not overlap in time (they share the workspace).
+ *  - Return value: GMM_OK (0) or a negative gmm_status_t.  Argument errors are
+ *    found on the host before anything is enqueued.  Device-side conditions
+ *    (non-finite or non-positive parameters, a synchronisation wait that ran
+ *    out) are recorded in a device status word; they are returned by the call
+ *    itself when it synchronises (loglik_on_host), otherwise by
+ *    gmm_stream_status().  gmm_last_error() gives the message of the last
+ *    failure on the calling thread.  There is no fallback path: a failure is
+ *    reported, never silently computed another way.
+ */
+#ifndef GMM_B300_H
+#define GMM_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GMM_SPHERICAL = 0, GMM_DIAG = 1 } gmm_cov_t;
+typedef enum { GMM_F32 = 0, GMM_BF16 = 1 } gmm_dtype_t;
+
+/* Arithmetic of the two tensor-core contractions (logits and statistics).
+ *  FAST:    half-precision (fp16) operands with fp32 accumulation, one pass.
+ *           Data are scaled by a power of two so that |x|^2 fits fp16 (bf16
+ *           data then stay exact); float32 data are also shifted by the mean
+ *           of the component means.
+ *  PRECISE: every operand split into two fp16 parts (hi + lo, 22 significant
+ *           bits), three products per contraction (hi*hi + hi*lo + lo*hi),
+ *           fp32 accumulation; data shifted and scaled as above.
+ *  AUTO:    FAST for bf16 X, PRECISE for float32 X. */
+typedef enum { GMM_PREC_AUTO = 0, GMM_PREC_FAST = 1, GMM_PREC_PRECISE = 2 } gmm_precision_t;
+
+typedef enum {
+    GMM_OK = 0,
+    GMM_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, N < 1, D < 1, ... */
+    GMM_ERR_UNSUPPORTED = -2,   /* a shape outside the supported window */
+    GMM_ERR_NONFINITE = -3,     /* a parameter is NaN/inf, or a variance <= 0 */
+    GMM_ERR_CUDA = -4,          /* a CUDA runtime call failed */
+    GMM_ERR_TIMEOUT = -5,       /* a device-side wait exceeded its bound */
+    GMM_ERR_RANGE = -6          /* data too large for the FAST operand range */
+} gmm_status_t;
+
+typedef struct {
+    int32_t precision;       /* gmm_precision_t, default AUTO */
+    float reg_covar;         /* added to every new variance, default 1e-6 */
+    float var_floor;         /* new variance = max(v, var_floor) + reg_covar, default 0 */
+    float x_absmax;          /* > 0: caller's bound on max |X| (skips a scan of X) */
+    int32_t loglik_on_host;  /* 1: total_loglik is a host pointer; the call waits
+                                for the stream and reports device-side errors */
+} gmm_opts;
+
+/* Fill *opts with the defaults listed above. */
+void gmm_default_opts(gmm_opts *opts);
+
+/*
+ * One EM iteration ("Flash-GMM", section 2; "ML0094 GMM vs K-Means").
+ *   E-step: r_ik = pi_k N(x_i | mu_k, Sigma_k) / sum_j pi_j N(x_i | mu_j, Sigma_j)
+ *   M-step: N_k = sum_i r_ik;  new log-weight = log(N_k / N);
+ *           new mean mu_k' = sum_i r_ik x_i / N_k;
+ *           diagonal:  s2_kd' = sum_i r_ik (x_id - mu_kd')^2 / N_k
+ *           spherical: s2_k'  = sum_i r_ik ||x_i - mu_k'||^2 / (D N_k)
+ *           then s2' = max(s2', var_floor) + reg_covar.
+ *   A component with N_k < 1e-30 keeps its mean and variance; its new
+ *   log-weight is -inf.
+ *   total_loglik = sum_i log sum_k pi_k N(x_i | mu_k, Sigma_k), evaluated at
+ *   the INPUT parameters (a by-product of the E-step), as one double; a
+ *   device pointer unless opts->loglik_on_host.
+ * Outputs may alias the corresponding inputs (all inputs are consumed before
+ * the first output is written).  Statistics are reduced in a fixed order:
+ * repeated calls give bit-identical results.
+ * Supported: 1 <= D <= 128, 1 <= K <= 8192 (K <= 1024 in a single pass over
+ * X; above that the E-step's normaliser is computed in a first pass and kept
+ * in an N-float buffer), N >= 1; PRECISE needs D <= 64.
+ */
+int gmm_em_step(const void *X, int64_t N, int32_t D, int32_t K, int32_t cov_type,
+                int32_t x_dtype, const float *log_weights, const float *means,
+                const float *vars, float *new_log_weights, float *new_means,
+                float *new_vars, double *total_loglik, const gmm_opts *opts,
+                void *stream);
+
+/*
+ * Top-m soft assignment (the multi-assignment of "Flash-GMM", conclusion:
+ * boundary vectors go to several posting lists, read off the final
+ * responsibilities).  For every point i, resp_out[i*m + j] and
+ * idx_out[i*m + j] (j < m) are its j-th largest responsibility r_ik
+ * (normalised over all K components, not over the m kept) and the component
+ * index k, in descending order of r; equal responsibilities are ordered by
+ * the lower index first.  m = 1 is the hard label (predict).  total_loglik
+ * (may be NULL) receives sum_i log p(x_i) as in gmm_em_step.
+ * Supported: 1 <= m <= min(K, 16); other limits as gmm_em_step.
+ */
+int gmm_predict_topm(const void *X, int64_t N, int32_t D, int32_t K, int32_t cov_type,
+                     int32_t x_dtype, const float *log_weights, const float *means,
+                     const float *vars, int32_t m, float *resp_out, int32_t *idx_out,
+                     double *total_loglik, const gmm_opts *opts, void *stream);
+
+/* Bytes of internal workspace a call with these arguments needs. */
+size_t gmm_workspace_bytes(int64_t N, int32_t D, int32_t K, int32_t cov_type,
+                           int32_t x_dtype, const gmm_opts *opts);
+
+/* Allocate the workspace for such calls now (on the current device). */
+int gmm_reserve(int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
+                const gmm_opts *opts);
+
+/* Wait for `stream` and return the device-side status of the calls enqueued
+ * on it so far (GMM_OK, GMM_ERR_NONFINITE, GMM_ERR_TIMEOUT, GMM_ERR_RANGE),
+ * then clear it. */
+int gmm_stream_status(void *stream);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char *gmm_last_error(void);
+
+/* Free the internal workspace of every device (call when idle). */
+void gmm_release(void);
+
+/* Number of kernel launches the last successful call enqueued. */
+int32_t gmm_last_launch_count(void);
+
+/* Timing of the main (fused E-step + statistics) kernel, for measurement:
+ * after gmm_profile_begin(), each call on this thread records a CUDA event
+ * pair around every launch of that kernel on its stream; gmm_profile_end()
+ * waits for those events and returns the summed device time in milliseconds
+ * and the number of launches, then stops recording. */
+void gmm_profile_begin(void);
+int gmm_profile_end(double *main_kernel_ms, int32_t *launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GMM_B300_H */

@@ -1,0 +1,60 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/gmm.h declares, rejects bad arguments before touching
+the device, and plans a workspace that does not grow with N (the O(K D)
+memory claim) while a naive EM's responsibility matrix would."""
+import ctypes
+import os
+
+import pytest
+
+import em_gmm_step_02_b300 as G
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "naive_footprint.txt")
+
+
+def test_library_exports_every_declared_symbol():
+    lib = G.lib()
+    names = G.declared_symbols()
+    assert "gmm_em_step" in names and "gmm_predict_topm" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_default_opts():
+    o = G.gmm_default_opts()
+    assert o.precision == 0 and o.loglik_on_host == 0
+    assert abs(o.reg_covar - 1e-6) < 1e-12 and o.var_floor == 0.0 and o.x_absmax == 0.0
+
+
+def _call(N=100, D=8, K=4, cov=1, dt=0, X=0x1000, p=0x2000, ll=0x3000, opts=None):
+    o = opts or G.gmm_default_opts()
+    vp = ctypes.c_void_p
+    return G.lib().gmm_em_step(vp(X), N, D, K, cov, dt, vp(p), vp(p), vp(p), vp(p), vp(p), vp(p),
+                               vp(ll), ctypes.byref(o), vp(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=0), -1), (dict(D=0), -1), (dict(K=0), -1), (dict(cov=2), -1), (dict(dt=3), -1),
+    (dict(X=0), -1), (dict(X=0x1004), -1), (dict(p=0x2002), -1), (dict(ll=0), -1),
+    (dict(D=129), -2), (dict(K=8193), -2), (dict(D=65, dt=0), -2),
+])
+def test_argument_errors_are_found_on_the_host(kw, code):
+    assert _call(**kw) == code
+    assert G.gmm_last_error() != ""
+
+
+def test_bad_options_rejected():
+    assert _call(opts=G.gmm_default_opts(precision=7)) == -1
+    assert _call(opts=G.gmm_default_opts(reg_covar=-1.0)) == -1
+    assert _call(opts=G.gmm_default_opts(var_floor=float("nan"))) == -1
+
+
+def test_workspace_is_independent_of_N_and_far_below_naive_footprint():
+    # page numbers: N = 10M, D = 128, K = 2048 at 4 bytes -> R about 80 GB, X about 5 GB
+    N, D, K, bpv, r_gb, x_gb = [float(v) for v in open(GOLDEN).read().split("\n")[-2].split()]
+    assert abs(N * K * bpv / 1e9 - r_gb) / r_gb < 0.05
+    assert abs(N * D * bpv / 1e9 - x_gb) / x_gb < 0.05
+    a = G.gmm_workspace_bytes(1_000_000, 128, 1024, "diag", "bf16")
+    b = G.gmm_workspace_bytes(100_000_000, 128, 1024, "diag", "bf16")
+    assert a == b > 0
+    assert b < 10_000_000 * 1024 * 4 / 100      # < 1% of the N x K matrix at N = 10M

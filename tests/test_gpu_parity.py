@@ -1,0 +1,213 @@
+"""Parity of the CUDA EM step (through the C ABI) with the float64 oracle.
+
+Tolerances follow the method's stated accuracy targets:
+  PRECISE (float32 data): per-component relative L2 error of means, variances
+      and of the weight vector <= 1e-4; per-point mean log-likelihood within
+      1e-4 (absolute).
+  FAST (bf16 data): <= 2e-2 relative and 1e-2 (absolute) per-point mean
+      log-likelihood; the log-likelihood after 20 iterations within 1e-3
+      relative.
+Variances are compared on components holding at least MIN_NK effective
+points.  Below that a variance is a difference of two nearly equal moments of
+one or two points and carries no stable relative digits in either
+implementation; for those components the raw second moment (s2 + mu^2) is
+compared instead, with the same tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import em_gmm_step_02_b300 as G
+import oracle
+import workloads as W
+from gpu_util import params_to_device, rel_l2_rows
+
+TOL = {"precise": (1e-4, 1e-4), "fast": (2e-2, 1e-2)}
+MIN_NK = 16.0
+
+
+def run_gpu(X_cpu, lw, mu, var, cov, precision="auto", **kw):
+    X = X_cpu.cuda()
+    lw_d, mu_d, var_d = params_to_device(lw, mu, var)
+    out = G.gmm_em_step(X, lw_d, mu_d, var_d, cov, precision=precision, **kw)
+    torch.cuda.synchronize()
+    assert G.gmm_stream_status() == 0
+    return [t.cpu().numpy() for t in out[:3]] + [float(out[3].item())]
+
+
+def compare(got, ref, N, cov, path):
+    tol, tol_ll = TOL[path]
+    lw_g, mu_g, var_g, ll_g = got
+    lw_r, mu_r, var_r, ll_r = ref
+    K = len(lw_r)
+    e_w = np.linalg.norm(np.exp(lw_g) - np.exp(lw_r)) / np.linalg.norm(np.exp(lw_r))
+    e_mu = rel_l2_rows(mu_g, mu_r).max()
+    vg = np.asarray(var_g, np.float64).reshape(K, -1)
+    vr = np.asarray(var_r, np.float64).reshape(K, -1)
+    big = np.exp(lw_r) * N >= MIN_NK
+    e_var = rel_l2_rows(vg[big], vr[big]).max() if big.any() else 0.0
+    m2g = vg + (mu_g.astype(np.float64) ** 2 if cov == "diag" else (mu_g.astype(np.float64) ** 2).mean(1, keepdims=True))
+    m2r = vr + (mu_r ** 2 if cov == "diag" else (mu_r ** 2).mean(1, keepdims=True))
+    e_m2 = rel_l2_rows(m2g, m2r).max()
+    e_ll = abs(ll_g - ll_r) / N
+    msg = (f"w {e_w:.2e} mu {e_mu:.2e} var {e_var:.2e} ({big.sum()}/{K} comps) m2 {e_m2:.2e} "
+           f"ll/N {e_ll:.2e} (tol {tol}, {tol_ll})")
+    assert e_w <= tol and e_mu <= tol and e_var <= tol and e_m2 <= tol and e_ll <= tol_ll, msg
+    return msg
+
+
+def one_step_case(w, rows=None, precision="auto", path=None):
+    X = W.make_data(w, rows)
+    init = W.make_init(w, X)
+    ref = oracle.em_step(X.float().numpy(), *init, w.cov)
+    got = run_gpu(X, *init, w.cov, precision)
+    if path is None:
+        path = "fast" if (precision == "fast" or (precision == "auto" and w.x_dtype == "bf16")) else "precise"
+    return compare(got, ref, X.shape[0], w.cov, path)
+
+
+# --------------------------------------------------------------------------- small shapes
+CASES = [
+    # N, D, K, cov, x_dtype, precision
+    (4096, 8, 16, "diag", "f32", "auto"),
+    (3001, 63, 40, "diag", "f32", "auto"),
+    (1000, 1, 3, "diag", "f32", "auto"),
+    (3777, 17, 129, "spherical", "f32", "auto"),
+    (5000, 64, 256, "spherical", "f32", "auto"),
+    (3001, 96, 200, "diag", "bf16", "auto"),
+    (20000, 128, 1024, "diag", "bf16", "auto"),
+    (1500, 8, 1, "diag", "bf16", "auto"),
+    (2500, 100, 300, "diag", "f32", "fast"),
+    (12000, 32, 1100, "diag", "bf16", "auto"),
+    (129, 5, 7, "spherical", "bf16", "auto"),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N,D,K,cov,xd,prec", CASES)
+def test_one_step_small(N, D, K, cov, xd, prec):
+    w = W.generic(N, D, K, cov, xd, seed=N + D + K)
+    print(one_step_case(w, precision=prec))
+
+
+@pytest.mark.gpu
+def test_tiny_workload_20_iterations():
+    w = W.WORKLOADS["tiny_diag"]
+    X = W.make_data(w)
+    lw, mu, var = W.make_init(w, X)
+    Xf = X.numpy()
+    ref_lls = []
+    ref = (lw.astype(np.float64), mu.astype(np.float64), var.astype(np.float64))
+    for _ in range(w.iters):
+        *ref, ll = oracle.em_step(Xf, *ref, w.cov)
+        ref_lls.append(ll)
+    Xd = X.cuda()
+    p = params_to_device(lw, mu, var)
+    lls = []
+    for _ in range(w.iters):
+        *p, ll = G.gmm_em_step(Xd, *p, w.cov)
+        lls.append(float(ll.item()))
+    got = [t.cpu().numpy() for t in p]
+    N = X.shape[0]
+    assert np.abs(np.asarray(lls) - np.asarray(ref_lls)).max() / N <= 1e-4, (lls, ref_lls)
+    assert rel_l2_rows(got[1], ref[1]).max() <= 1e-4
+
+
+# --------------------------------------------------------------------------- workload prefixes
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,rows", [
+    ("spherical_1m", 20000),
+    ("embed_10m", 20000),
+    ("descriptor_100m", 20000),
+    ("largek_2m", 30000),
+])
+def test_workload_prefix_one_step(name, rows):
+    w = W.WORKLOADS[name]
+    prec = "fast" if name == "descriptor_100m" else "auto"
+    print(one_step_case(w.scaled(rows), precision=prec))
+
+
+@pytest.mark.gpu
+def test_embed_prefix_20_iterations_ll():
+    w = W.WORKLOADS["embed_10m"].scaled(20000)
+    X = W.make_data(w)
+    lw, mu, var = W.make_init(w, X)
+    *_, ref_lls = oracle.em_run(X.float().numpy(), lw, mu, var, w.cov, 20)
+    Xd = X.cuda()
+    p = params_to_device(lw, mu, var)
+    for _ in range(20):
+        *p, ll = G.gmm_em_step(Xd, *p, w.cov)
+    got = float(ll.item())
+    assert abs(got - ref_lls[-1]) / abs(ref_lls[-1]) <= 1e-3, (got, ref_lls[-1])
+
+
+# --------------------------------------------------------------------------- properties
+@pytest.mark.gpu
+def test_outputs_may_alias_inputs_and_runs_are_deterministic():
+    w = W.generic(3000, 40, 300, "diag", "bf16", seed=5)
+    X = W.make_data(w).cuda()
+    init = W.make_init(w, X.cpu())
+    a = params_to_device(*init)
+    b = params_to_device(*init)
+    r1 = G.gmm_em_step(X, *a, w.cov)
+    G.gmm_em_step(X, *b, w.cov, out=b)        # in place
+    torch.cuda.synchronize()
+    for x, y in zip(r1[:3], b):
+        assert torch.equal(x, y)
+    r2 = G.gmm_em_step(X, *a, w.cov)
+    for x, y in zip(r1, r2):
+        assert torch.equal(x, y)
+
+
+@pytest.mark.gpu
+def test_dead_component_keeps_parameters():
+    w = W.generic(2000, 16, 20, "diag", "f32", seed=9)
+    X = W.make_data(w)
+    lw, mu, var = W.make_init(w, X)
+    lw = lw.copy()
+    lw[3] = -np.inf
+    got = run_gpu(X, lw, mu, var, "diag")
+    assert got[0][3] == -np.inf
+    np.testing.assert_array_equal(got[1][3], mu[3])
+    np.testing.assert_array_equal(got[2][3], var[3])
+    ref = oracle.em_step(X.numpy(), lw, mu, var, "diag")
+    keep = [k for k in range(20) if k != 3]
+    assert rel_l2_rows(got[1][keep], ref[1][keep]).max() < 1e-4
+
+
+@pytest.mark.gpu
+def test_nonpositive_variance_is_reported():
+    w = W.generic(500, 4, 3, "diag", "f32", seed=1)
+    X = W.make_data(w).cuda()
+    lw, mu, var = W.make_init(w, X.cpu())
+    var = var.copy()
+    var[1, 2] = 0.0
+    G.gmm_em_step(X, *params_to_device(lw, mu, var), "diag")
+    assert G.gmm_stream_status() == -3
+    assert G.gmm_stream_status() == 0     # status is cleared once read
+
+
+@pytest.mark.gpu
+def test_conservation_of_moments_full_size_embed():
+    """Full 10M x 128 x 1024 workload in the benchmark's launch configuration:
+    properties that hold at any size (weights sum to 1; sum_k N_k mu_k equals
+    the data sum; sum_k N_k (s2_k + mu_k^2) equals the sum of squares)."""
+    w = W.WORKLOADS["embed_10m"]
+    X = W.make_data(w, device="cuda")
+    lw, mu, var = W.make_init(w, X)
+    p = params_to_device(lw, mu, var)
+    lw2, mu2, var2, ll = G.gmm_em_step(X, *p, w.cov)
+    torch.cuda.synchronize()
+    assert G.gmm_stream_status() == 0
+    N = X.shape[0]
+    pi = torch.exp(lw2.double())
+    assert abs(pi.sum().item() - 1.0) < 1e-5
+    Nk = pi * N
+    s1 = (Nk[:, None] * mu2.double()).sum(0)
+    xs = X.double().sum(0)
+    scale = X.double().abs().sum(0)
+    assert ((s1 - xs).abs() / scale).max().item() < 2e-3
+    s2 = (Nk[:, None] * (var2.double() - 1e-6 + mu2.double() ** 2)).sum(0)
+    x2 = (X.double() ** 2).sum(0)
+    assert ((s2 - x2).abs() / x2).max().item() < 2e-2
+    assert np.isfinite(ll.item())
