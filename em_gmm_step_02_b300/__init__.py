@@ -56,6 +56,8 @@ def lib():
         L.gmm_em_step.argtypes = [vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
                                   ctypes.POINTER(gmm_opts), vp]
         L.gmm_em_step.restype = ctypes.c_int
+        L.gmm_em_step_noalloc.argtypes = L.gmm_em_step.argtypes
+        L.gmm_em_step_noalloc.restype = ctypes.c_int
         L.gmm_predict_topm.argtypes = [vp, i64, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp,
                                        ctypes.POINTER(gmm_opts), vp]
         L.gmm_predict_topm.restype = ctypes.c_int
@@ -161,6 +163,28 @@ def gmm_em_step(X, log_weights, means, vars_, cov="diag", *, out=None, opts: gmm
                            _dev(ll, "total_loglik", torch.float64), ctypes.byref(opts), _stream(stream))
     _check(rc)
     return out[0], out[1], out[2], ll
+
+
+def gmm_em_step_noalloc(X, log_weights, means, vars_, cov="diag", *, out, opts: gmm_opts | None = None,
+                        stream=None, **opt_kw):
+    """The EM step without any device allocation inside the library (see
+    gmm_em_step_noalloc in include/gmm.h).  ``out`` = (new_log_weights,
+    new_means, new_vars, total_loglik) must be given: the caller provides all
+    memory.  Returns ``out``."""
+    N, D, K, cov_i, dt = _shape(X, means, cov)
+    if opts is None:
+        opts = gmm_default_opts(**opt_kw)
+    opts.loglik_on_host = 0
+    rc = lib().gmm_em_step_noalloc(_dev(X, "X"), N, D, K, cov_i, dt,
+                                   _dev(log_weights, "log_weights", torch.float32),
+                                   _dev(means, "means", torch.float32), _dev(vars_, "vars", torch.float32),
+                                   _dev(out[0], "new_log_weights", torch.float32),
+                                   _dev(out[1], "new_means", torch.float32),
+                                   _dev(out[2], "new_vars", torch.float32),
+                                   _dev(out[3], "total_loglik", torch.float64), ctypes.byref(opts),
+                                   _stream(stream))
+    _check(rc)
+    return out
 
 
 def gmm_predict_topm(X, log_weights, means, vars_, cov="diag", m=1, *, opts: gmm_opts | None = None,

@@ -540,3 +540,117 @@ void gmm_release(void) {
 }
 
 }  // extern "C"
+
+// ====================================================================== no-allocation variant
+// gmm_em_step_noalloc: the single-pass EM step with all of its scratch taken
+// from one fixed device array that is part of this library's module, for
+// callers that must not call cudaMalloc/cudaFree while they run.
+//
+// The array is a file-scope __device__ variable, so every GPU that loads the
+// library reserves kNoAllocScratchBytes for it until the process exits.  Host
+// code cannot use the variable's name as a device address; its address on
+// each device is looked up once with cudaGetSymbolAddress (on the first call
+// made with that device current) and cached.
+constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;   // 40 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+uint8_t* g_noalloc_base[kNoAllocMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Address of the scratch array on the current device (looked up once).
+int noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(GMM_ERR_UNSUPPORTED, "device index too large");
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_base[dev]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr)
+      return fail(GMM_ERR_CUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
+    g_noalloc_base[dev] = static_cast<uint8_t*>(ptr);
+  }
+  *out = g_noalloc_base[dev];
+  return GMM_OK;
+}
+}  // namespace
+
+extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type,
+                                   int32_t x_dtype, const float* log_weights, const float* means,
+                                   const float* vars, float* new_log_weights, float* new_means,
+                                   float* new_vars, double* total_loglik, const gmm_opts* opts,
+                                   void* stream) {
+  g_launches = 0;
+  gmm_opts o;
+  gmm_default_opts(&o);
+  if (opts) o = *opts;
+  if (!X) return fail(GMM_ERR_INVALID_ARG, "X is NULL");
+  int r;
+  if ((r = check_ptr(log_weights, "log_weights")) || (r = check_ptr(means, "means")) ||
+      (r = check_ptr(vars, "vars")) || (r = check_ptr(new_log_weights, "new_log_weights")) ||
+      (r = check_ptr(new_means, "new_means")) || (r = check_ptr(new_vars, "new_vars")))
+    return r;
+  if (!total_loglik) return fail(GMM_ERR_INVALID_ARG, "total_loglik is NULL");
+  Plan p;
+  if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
+  if (p.two_pass)
+    return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_noalloc supports K <= 1024 (larger K needs an N-sized buffer)");
+
+  // Scratch layout inside the fixed array; the number of tile groups (and so
+  // of CTAs) is lowered until the per-group statistics fit.
+  const size_t piece = static_cast<size_t>(2 * p.nch) * kChunkBytes;
+  const size_t row_bytes = sizeof(double) * static_cast<size_t>(p.K_pad) * p.F;
+  size_t fixed = kStatusBytes + align256(sizeof(Meta)) + 256 +
+                 align256(static_cast<size_t>(p.n_slices) * p.np * piece) + 2 * align256(sizeof(float) * p.K_pad) +
+                 align256(sizeof(double) * kCombineBlocks);
+  if (fixed + align256(row_bytes) > kNoAllocScratchBytes)
+    return fail(GMM_ERR_UNSUPPORTED, "problem too large for the 40 MiB scratch of gmm_em_step_noalloc");
+  const int tg_fit = static_cast<int>((kNoAllocScratchBytes - fixed) / row_bytes);
+  p.tg = std::max(1, std::min(p.tg, tg_fit));
+  size_t off = kStatusBytes;
+  p.off_meta = off; off += align256(sizeof(Meta));
+  p.off_ll = off; off += 256;
+  p.off_pimg = off; off += align256(static_cast<size_t>(p.n_slices) * p.np * piece);
+  p.off_cadj = off; off += align256(sizeof(float) * p.K_pad);
+  p.off_iscale = off; off += align256(sizeof(float) * p.K_pad);
+  p.off_llpart = off; off += align256(sizeof(double) * std::max<size_t>(p.tg, kCombineBlocks));
+  p.off_part = off; off += align256(row_bytes * p.tg);
+  p.off_lsepart = p.off_lse = off;
+  if (off > kNoAllocScratchBytes) return fail(GMM_ERR_UNSUPPORTED, "scratch layout overflow");
+
+  uint8_t* ws = nullptr;
+  if ((r = noalloc_scratch(&ws))) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  if ((r = set_smem_attr(fn, p.smem))) return r;
+  // the array keeps the previous call's contents: clear the status word and
+  // the statistics accumulators, which must start at zero
+  CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(uint32_t), s));
+  if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
+  CUDA_TRY(cudaMemsetAsync(ws + p.off_part, 0, row_bytes * p.tg, s));
+  FusedArgs a = base_args(p, X, ws);
+  a.mode = MODE_EM;
+  a.C = p.C;
+  if ((r = launch(fn, dim3(p.C * p.tg, 1), dim3(416), p.smem, s, p.C, a))) return r;
+  double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
+  {
+    float reg = o.reg_covar, floor_ = o.var_floor;
+    int Dp = p.nch * kAtomElems;
+    if ((r = launch(kernel_handle(K_FINALIZE), dim3(p.K), dim3(128), 0, s, 1,
+                    static_cast<const double*>(a.part), p.tg, p.K_pad, p.F, Dp, p.D, p.K, p.N, p.cov_diag, reg,
+                    floor_, 32768.0, static_cast<const Meta*>(a.meta),
+                    reinterpret_cast<const double*>(ws + p.off_llpart), p.tg, new_log_weights, new_means,
+                    new_vars, means, vars, ll_dev)))
+      return r;
+  }
+  if (o.loglik_on_host) {
+    CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    uint32_t st = 0;
+    CUDA_TRY(cudaMemcpy(&st, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    if (st) return status_to_code(st);
+  }
+  return GMM_OK;
+}

@@ -130,6 +130,37 @@ int gmm_predict_topm(const void *X, int64_t N, int32_t D, int32_t K, int32_t cov
                      const float *vars, int32_t m, float *resp_out, int32_t *idx_out,
                      double *total_loglik, const gmm_opts *opts, void *stream);
 
+/*
+ * gmm_em_step_noalloc -- the same EM step as gmm_em_step, for callers that
+ * cannot allocate device memory while they run: for example a process whose
+ * device memory is handed out up front by its own allocator, or a code path
+ * that must not call cudaMalloc/cudaFree because those calls can synchronise
+ * the whole device.  The web pages describing the method have no counterpart
+ * of this entry point.
+ *  - Allocates nothing.  All scratch comes from one 40 MiB array compiled into
+ *    this library; every GPU that loads the library keeps those 40 MiB
+ *    reserved until the process exits.  The caller passes inputs and outputs
+ *    exactly as for gmm_em_step.
+ *  - Limits: K <= 1024 (larger K needs an N-sized buffer) and the statistics
+ *    of the problem must fit the array; when they fit only partly the step
+ *    runs on fewer thread blocks.  Larger problems are rejected with
+ *    GMM_ERR_UNSUPPORTED and a message in gmm_last_error().
+ *  - The first call with a given device current looks up the array's device
+ *    address (cudaGetSymbolAddress) and sets kernel attributes; make that
+ *    first call before any stream capture.
+ *  - All calls share the one array, and it keeps the last call's contents
+ *    (each call clears the parts that must start at zero).  Calls whose work
+ *    overlaps on the GPU, on any streams, race on that array: serialise them.
+ *  - Device-side conditions (non-finite parameters, timeouts) are reported
+ *    only when opts->loglik_on_host is set (the call then waits for the
+ *    stream); gmm_stream_status() does not see them.
+ */
+int gmm_em_step_noalloc(const void *X, int64_t N, int32_t D, int32_t K, int32_t cov_type,
+                        int32_t x_dtype, const float *log_weights, const float *means,
+                        const float *vars, float *new_log_weights, float *new_means,
+                        float *new_vars, double *total_loglik, const gmm_opts *opts,
+                        void *stream);
+
 /* Bytes of internal workspace a call with these arguments needs. */
 size_t gmm_workspace_bytes(int64_t N, int32_t D, int32_t K, int32_t cov_type,
                            int32_t x_dtype, const gmm_opts *opts);

@@ -1,0 +1,70 @@
+"""gmm_em_step_noalloc, the EM step for callers that cannot allocate device
+memory while they run (their memory is reserved up front, or cudaMalloc's
+implicit device synchronisation is not allowed on their path).  It must give
+the same result as gmm_em_step, within the tolerances of the parity tests,
+on two calls in a row that share its fixed scratch array, and must not change
+the amount of free device memory.
+
+This file is named to be collected last."""
+import numpy as np
+import pytest
+import torch
+
+import em_gmm_step_02_b300 as G
+import workloads as W
+from gpu_util import params_to_device, rel_l2_rows
+
+CASES = [
+    # N, D, K, cov, x_dtype, (tolerance on means/variances/weights, on log-likelihood per point)
+    (20000, 128, 1024, "diag", "bf16", (2e-2, 1e-2)),
+    (5000, 64, 256, "spherical", "f32", (1e-4, 1e-4)),
+]
+
+
+def _close(a, b, N, tol, tol_ll):
+    lw_a, mu_a, var_a, ll_a = [t.cpu().numpy().astype(np.float64) for t in a]
+    lw_b, mu_b, var_b, ll_b = [t.cpu().numpy().astype(np.float64) for t in b]
+    K = len(lw_a)
+    assert np.linalg.norm(np.exp(lw_a) - np.exp(lw_b)) / np.linalg.norm(np.exp(lw_b)) <= tol
+    assert rel_l2_rows(mu_a, mu_b).max() <= tol
+    assert rel_l2_rows(var_a.reshape(K, -1), var_b.reshape(K, -1)).max() <= tol
+    assert abs(ll_a[0] - ll_b[0]) / N <= tol_ll
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N,D,K,cov,xd,tols", CASES)
+def test_noalloc_matches_em_step_on_two_calls(N, D, K, cov, xd, tols):
+    w = W.generic(N, D, K, cov, xd, seed=11)
+    X = W.make_data(w).cuda()
+    init = W.make_init(w, X.cpu())
+    p = params_to_device(*init)
+    ref = G.gmm_em_step(X, *p, cov)
+    torch.cuda.synchronize()
+    outs = []
+    for call in range(2):
+        out = (torch.empty_like(p[0]), torch.empty_like(p[1]), torch.empty_like(p[2]),
+               torch.empty(1, dtype=torch.float64, device="cuda"))
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
+        G.gmm_em_step_noalloc(X, *p, cov, out=out)
+        torch.cuda.synchronize()
+        free_after = torch.cuda.mem_get_info()[0]
+        if call == 1:
+            assert free_after == free_before
+        _close(out, ref, N, *tols)
+        outs.append(out)
+    # the second call sees the first call's leftovers in the shared array
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_large_k():
+    X = torch.zeros((256, 8), dtype=torch.bfloat16, device="cuda")
+    K = 2048
+    p = params_to_device(np.zeros(K), np.zeros((K, 8)), np.ones((K, 8)))
+    out = (torch.empty_like(p[0]), torch.empty_like(p[1]), torch.empty_like(p[2]),
+           torch.empty(1, dtype=torch.float64, device="cuda"))
+    with pytest.raises(G.GmmError) as e:
+        G.gmm_em_step_noalloc(X, *p, "diag", out=out)
+    assert e.value.code == -2
