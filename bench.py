@@ -304,12 +304,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="embed_10m", choices=sorted(W.WORKLOADS))
     ap.add_argument("--precision", default="auto", choices=["auto", "fast", "precise"])
+    ap.add_argument("--rows", type=int, default=0,
+                    help="run on the first ROWS rows of the workload (profiling a smaller case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
+    if args.rows > 0:
+        w = w.scaled(min(args.rows, w.N))
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, w, ws, rank)
