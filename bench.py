@@ -227,6 +227,24 @@ def run_ours(args, w, ws, rank, local):
     status = G.gmm_stream_status()
     assert status == 0, G.gmm_last_error()
 
+    # the workload's final top-m soft assignment, timed on its own
+    topm = None
+    if w.topm > 0 and not args.no_topm:
+        G.gmm_predict_topm(X, *p, w.cov, w.topm, opts=opts)
+        torch.cuda.synchronize(dev)
+        assert G.gmm_stream_status() == 0, G.gmm_last_error()
+        reps = 3
+        e0.record(stream)
+        for _ in range(reps):
+            G.gmm_predict_topm(X, *p, w.cov, w.topm, opts=opts)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_ms = e0.elapsed_time(e1) / reps
+        topm = {"m": w.topm, "ms": t_ms, "points_per_s": w.N * 1e3 / t_ms,
+                "logit_tflops": 4.0 * w.N * w.K * w.D / (t_ms * 1e-3) / 1e12,
+                "job_ms": w.iters * ms + t_ms,
+                "job": f"{w.iters} EM iterations + top-{w.topm}"}
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -283,6 +301,8 @@ def run_ours(args, w, ws, rank, local):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if topm is not None:
+        line["topm"] = topm
     if not args.no_cpu and ws == 1:
         import oracle
         cap = min(w.N, 400_000)
@@ -308,6 +328,7 @@ def main():
                     help="run on the first ROWS rows of the workload (profiling a smaller case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-topm", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     args = ap.parse_args()

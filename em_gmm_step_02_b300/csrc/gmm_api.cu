@@ -81,7 +81,7 @@ namespace {
 
 template <int NP, int NCH, int NST>
 constexpr size_t cfg_smem() {
-  return Cfg<NP, NCH, NST>::kOffSmall + sizeof(Small) + 1024;   // + base alignment slack
+  return Cfg<NP, NCH, NST>::kEnd + 1024;   // + base alignment slack
 }
 
 size_t fused_smem(int np, int nch, int nst) {
@@ -109,6 +109,11 @@ int max_clusters(const void* fn, size_t smem, int C) {
   if (it != cache.end()) return it->second;
   int sms = device_sms();
   int n = std::max(1, sms / C);
+  // the occupancy query needs the kernel's dynamic shared-memory limit raised first
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess) {
+    cudaGetLastError();
+    return n;
+  }
   if (C > 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C * n, 1, 1);
@@ -159,7 +164,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
   p.smem = fused_smem(p.np, p.nch, p.nst);
   p.F = 2 * p.nch * kAtomElems + 1;
-  p.flush = p.fast ? 64 : 16;
+  p.flush = p.fast ? 128 : 16;
   const int sms = need_device ? device_sms() : 148;
   const void* fn = fused_fn(p.np, p.nch, p.nst);
   if (!p.two_pass) {
@@ -184,7 +189,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.off_cadj = off; off += align256(sizeof(float) * p.K_pad);
   p.off_iscale = off; off += align256(sizeof(float) * p.K_pad);
   p.off_part = off; off += align256(sizeof(double) * static_cast<size_t>(p.tg) * p.K_pad * p.F);
-  p.n_llpart = std::max<size_t>(p.tg, kCombineBlocks);
+  p.n_llpart = std::max<size_t>(static_cast<size_t>(p.tg) * p.C, kCombineBlocks);
   p.off_llpart = off; off += align256(sizeof(double) * p.n_llpart);
   p.off_lsepart = off;
   p.off_lse = off;
@@ -420,7 +425,7 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
   CUDA_TRY(cudaMemsetAsync(ws + p.off_part, 0, sizeof(double) * static_cast<size_t>(p.tg) * p.K_pad * p.F, s));
 
   FusedArgs a = base_args(p, X, ws);
-  int n_ll = p.tg;
+  int n_ll = p.tg * p.C;   // one log-likelihood partial per CTA
   if (!p.two_pass) {
     a.mode = MODE_EM;
     a.C = p.C;
@@ -470,9 +475,76 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
 int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
                      const float* log_weights, const float* means, const float* vars, int32_t m, float* resp_out,
                      int32_t* idx_out, double* total_loglik, const gmm_opts* opts, void* stream) {
-  (void)X; (void)N; (void)D; (void)K; (void)cov_type; (void)x_dtype; (void)log_weights; (void)means;
-  (void)vars; (void)m; (void)resp_out; (void)idx_out; (void)total_loglik; (void)opts; (void)stream;
-  return fail(GMM_ERR_UNSUPPORTED, "gmm_predict_topm is not available yet");
+  g_launches = 0;
+  gmm_opts o;
+  gmm_default_opts(&o);
+  if (opts) o = *opts;
+  if (!X) return fail(GMM_ERR_INVALID_ARG, "X is NULL");
+  int r;
+  if ((r = check_ptr(log_weights, "log_weights")) || (r = check_ptr(means, "means")) ||
+      (r = check_ptr(vars, "vars")) || (r = check_ptr(resp_out, "resp_out")) || (r = check_ptr(idx_out, "idx_out")))
+    return r;
+  if (o.loglik_on_host && !total_loglik) return fail(GMM_ERR_INVALID_ARG, "loglik_on_host needs total_loglik");
+  if (m < 1 || m > 16) return fail(GMM_ERR_UNSUPPORTED, "m must be in [1, 16]");
+  if (m > K) return fail(GMM_ERR_INVALID_ARG, "m must not exceed K");
+  Plan p;
+  if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
+  const int maxm = m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
+  const size_t smem = p.smem;   // the candidate lists live in the idle data stage / R area
+  // per-group candidate lists of the K > 1024 plan (after the EM workspace)
+  size_t off_gval = p.ws_bytes, off_gidx = p.ws_bytes, need = p.ws_bytes;
+  if (p.two_pass) {
+    const size_t lb = align256(sizeof(float) * static_cast<size_t>(p.n_kgroups) * N * m);
+    off_gidx = off_gval + lb;
+    need = off_gidx + lb;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = nullptr;
+  if ((r = get_workspace(need, &ws))) return r;
+  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  if ((r = set_smem_attr(fn, smem))) return r;
+  if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
+
+  FusedArgs a = base_args(p, X, ws);
+  a.mode = MODE_TOPM;
+  a.topm = m;
+  a.topm_max = maxm;
+  double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
+  if (!p.two_pass) {
+    a.C = p.C;
+    a.topm_groups = 1;
+    a.topm_val = resp_out;
+    a.topm_idx = idx_out;
+    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), smem, s, p.C, a))) return r;
+    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
+                              static_cast<const double*>(a.ll_part), p.tg * p.C, ll_dev)))
+      return r;
+  } else {
+    a.C = 8;
+    a.topm_groups = p.n_kgroups;
+    a.topm_val = reinterpret_cast<float*>(ws + off_gval);
+    a.topm_idx = reinterpret_cast<int32_t*>(ws + off_gidx);
+    if ((r = launch_main(fn, dim3(8 * p.tg1, p.n_kgroups), dim3(416), smem, s, 8, a))) return r;
+    if ((r = launch(kernel_handle(K_TOPM_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
+                    static_cast<const float*>(a.lse_part), static_cast<const float*>(a.topm_val),
+                    static_cast<const int32_t*>(a.topm_idx), p.n_kgroups, p.N, m, resp_out, idx_out,
+                    a.ll_part)))
+      return r;
+    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
+                              static_cast<const double*>(a.ll_part), kCombineBlocks, ll_dev)))
+      return r;
+  }
+  if (o.loglik_on_host) {
+    CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    uint32_t st = 0;
+    CUDA_TRY(cudaMemcpy(&st, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    if (st) {
+      CUDA_TRY(cudaMemset(ws, 0, sizeof(uint32_t)));
+      return status_to_code(st);
+    }
+  }
+  return GMM_OK;
 }
 
 int gmm_stream_status(void* stream) {
@@ -615,7 +687,7 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
   p.off_pimg = off; off += align256(static_cast<size_t>(p.n_slices) * p.np * piece);
   p.off_cadj = off; off += align256(sizeof(float) * p.K_pad);
   p.off_iscale = off; off += align256(sizeof(float) * p.K_pad);
-  p.off_llpart = off; off += align256(sizeof(double) * std::max<size_t>(p.tg, kCombineBlocks));
+  p.off_llpart = off; off += align256(sizeof(double) * std::max<size_t>(static_cast<size_t>(p.tg) * p.C, kCombineBlocks));
   p.off_part = off; off += align256(row_bytes * p.tg);
   p.off_lsepart = p.off_lse = off;
   if (off > kNoAllocScratchBytes) return fail(GMM_ERR_UNSUPPORTED, "scratch layout overflow");
@@ -641,7 +713,7 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
     if ((r = launch(kernel_handle(K_FINALIZE), dim3(p.K), dim3(128), 0, s, 1,
                     static_cast<const double*>(a.part), p.tg, p.K_pad, p.F, Dp, p.D, p.K, p.N, p.cov_diag, reg,
                     floor_, 32768.0, static_cast<const Meta*>(a.meta),
-                    reinterpret_cast<const double*>(ws + p.off_llpart), p.tg, new_log_weights, new_means,
+                    reinterpret_cast<const double*>(ws + p.off_llpart), p.tg * p.C, new_log_weights, new_means,
                     new_vars, means, vars, ll_dev)))
       return r;
   }

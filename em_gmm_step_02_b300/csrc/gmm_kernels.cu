@@ -65,6 +65,12 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t sq_f16x2(uint32_t x) {
+  __half2 h = *reinterpret_cast<__half2*>(&x);
+  h = __hmul2(h, h);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // ============================================================== scan of |X|
 __global__ void absmax_kernel(const void* __restrict__ X, int64_t n_elems, int x_bf16,
                               Meta* __restrict__ meta) {
@@ -227,9 +233,316 @@ __global__ void params_kernel(const float* __restrict__ log_weights, const float
   }
 }
 
+// ============================================================== top-m
+// MODE_TOPM work on one tile, after the row normaliser `lse` (log2 units,
+// over every component of the launch's K group) is known.  v[e] holds the
+// logit (log2 units) of component kbase + 64h + e for row nl; mh is the
+// maximum over those 64.
+//  1. Each half-row keeps its MAXM best components.  A candidate is ranked by
+//     the key (mh - logit) with its low six bits replaced by e: the order of
+//     keys is the order of logits, and equal truncated values fall back to
+//     the lower component index.  (Dropping six of the 23 mantissa bits moves
+//     a logit by at most 2^-17 of its distance to mh: well below the error of
+//     the logits themselves.)
+//  2. The lists of every half-row of every CTA in the cluster meet in shared
+//     memory; each CTA merges the rows r = rank (mod C): one warp per row, one
+//     lane per list, m rounds of a warp-wide maximum of the list heads.
+//  3. One K group: the final responsibilities 2^(logit - lse) and indices go
+//     to the output.  Several K groups: the group's best logits and indices
+//     go to the per-group buffers for the combine kernel.
+template <int MAXM>
+__device__ __forceinline__ void topm_tile(const FusedArgs& a, Small* S, uint8_t* lists, const float (&v)[64],
+                                          float mh, float lse, int64_t n0, int nl, int h, int lane, int warp,
+                                          int st, int rank, int C, int kbase, int j,
+                                          volatile uint32_t* abort_flag) {
+  float key[MAXM];
+#pragma unroll
+  for (int s = 0; s < MAXM; ++s) key[s] = __uint_as_float(0x7f7fffffu);
+  const bool live = mh > -CUDART_INF_F;
+#pragma unroll
+  for (int e = 0; e < 64; ++e) {
+    const float d = live ? fminf(mh - v[e], 1e30f) : 1e30f;
+    float c = __uint_as_float((__float_as_uint(d) & ~63u) | static_cast<uint32_t>(e));
+#pragma unroll
+    for (int s = 0; s < MAXM; ++s) {
+      const float lo = fminf(c, key[s]);
+      c = fmaxf(c, key[s]);
+      key[s] = lo;
+    }
+  }
+  float* lv = reinterpret_cast<float*>(lists);
+  uint16_t* li = reinterpret_cast<uint16_t*>(lists + kBN * 2 * MAXM * 4);
+  if (C > 1 && j > 0) mbar_wait_cluster(&S->tfree, (j - 1) & 1, abort_flag, a.status);
+#pragma unroll
+  for (int s = 0; s < MAXM; ++s) {
+    const uint32_t b = __float_as_uint(key[s]);
+    const float dd = __uint_as_float(b & ~63u);
+    lv[(nl * 2 + h) * MAXM + s] = dd >= 1e29f ? -CUDART_INF_F : mh - dd;
+    li[(nl * 2 + h) * MAXM + s] = static_cast<uint16_t>(kbase + 64 * h + static_cast<int>(b & 63u));
+  }
+  if (h == 0) S->lse_row[nl] = lse;
+  named_bar_sync(1, 256);
+  if (C > 1) {
+    if (st == 0) {
+      fence_acq_rel_cluster();
+      const uint32_t bar = smem_u32(&S->tready);
+      for (int r = 0; r < C; ++r) mbar_arrive_remote(mapa(bar, r));
+    }
+    mbar_wait_cluster(&S->tready, j & 1, abort_flag, a.status);
+  }
+  const int m = a.topm;
+  const int nlists = 2 * C;
+  const int w8 = warp - 4;
+  const uint32_t lv_s = smem_u32(lv), li_s = smem_u32(li);
+  for (int row = rank + C * w8; row < kBN; row += 8 * C) {
+    float hv[MAXM];
+    uint32_t hx[MAXM];
+    if (lane < nlists) {
+      const int cr = lane >> 1, hh = lane & 1;
+      const int base = (row * 2 + hh) * MAXM;
+      if (C > 1) {
+#pragma unroll
+        for (int s = 0; s < MAXM; ++s) {
+          hv[s] = ld_cluster_f32(mapa(lv_s + 4u * (base + s), cr));
+          hx[s] = ld_cluster_u16(mapa(li_s + 2u * (base + s), cr));
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < MAXM; ++s) {
+          hv[s] = lv[base + s];
+          hx[s] = li[base + s];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int s = 0; s < MAXM; ++s) {
+        hv[s] = -CUDART_INF_F;
+        hx[s] = 0xFFFFu;
+      }
+    }
+    float outv = -CUDART_INF_F;
+    uint32_t outi = 0xFFFFu;
+    for (int s = 0; s < m; ++s) {
+      float bv = hv[0];
+      uint32_t bi = hx[0];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const uint32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (lane < nlists && hx[0] == bi) {
+#pragma unroll
+        for (int u = 0; u + 1 < MAXM; ++u) {
+          hv[u] = hv[u + 1];
+          hx[u] = hx[u + 1];
+        }
+        hv[MAXM - 1] = -CUDART_INF_F;
+        hx[MAXM - 1] = 0xFFFFu;
+      }
+      if (lane == s) {
+        outv = bv;
+        outi = bi;
+      }
+    }
+    const int64_t n = n0 + row;
+    if (lane < m && n < a.N) {
+      if (a.topm_groups == 1) {
+        const float lse_r = S->lse_row[row];
+        a.topm_val[n * m + lane] = lse_r > -CUDART_INF_F ? ex2(outv - lse_r) : 0.f;
+        a.topm_idx[n * m + lane] = static_cast<int32_t>(outi);
+      } else {
+        const int64_t o = (static_cast<int64_t>(blockIdx.y) * a.N + n) * m + lane;
+        a.topm_val[o] = outv;
+        a.topm_idx[o] = static_cast<int32_t>(outi);
+      }
+    }
+  }
+  named_bar_sync(1, 256);
+  if (C > 1 && st == 0) {
+    const uint32_t bar = smem_u32(&S->tfree);
+    for (int r = 0; r < C; ++r) mbar_arrive_remote(mapa(bar, r));
+  }
+}
+
+// ============================================================== column sums
+// Sums v[0..63] over the 32 lanes of the warp, column by column, with a
+// halving butterfly: at each step a lane keeps one half of its columns and
+// receives its partner's values for them.  On return v[0] and v[1] of lane l
+// hold the sums of columns 2l and 2l + 1; the rest of v is overwritten.
+template <int L, int O>
+__device__ __forceinline__ void bfly_step(float (&v)[64], int lane) {
+  const bool up = (lane & O) != 0;
+#pragma unroll
+  for (int i = 0; i < L / 2; ++i) {
+    const float send = up ? v[i] : v[i + L / 2];
+    const float keep = up ? v[i + L / 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+  }
+}
+
+__device__ __forceinline__ void column_sums_32(float (&v)[64], int lane) {
+  bfly_step<64, 16>(v, lane);
+  bfly_step<32, 8>(v, lane);
+  bfly_step<16, 4>(v, lane);
+  bfly_step<8, 2>(v, lane);
+  bfly_step<4, 1>(v, lane);
+}
+
+// ============================================================== data transform
+// 16-byte load that bypasses L1 (each data tile is read once per SM).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// The four transform warps turn each 128-point tile of X into the two fp16
+// operand pieces [x' | x'^2] (PRECISE: hi and lo parts of each), with
+// x' = (x - shift) * scale, in the swizzled K-major layout of the data stage.
+// Thread `tid` owns one 8-feature unit of every RPP-th row.  All loads of a
+// tile are issued together (and, when the registers allow, one tile ahead)
+// so that the whole tile is in flight at once.
+template <typename CF, int NP, int NCH, int NST, bool XB>
+__device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm, Small* S,
+                                                volatile uint32_t* abort_flag, int tid, int tgroup,
+                                                int n_tgroups, int my_tiles) {
+  constexpr int UPR = 8 * NCH;               // 8-feature units per row
+  constexpr int RPP = 128 / UPR;             // rows per pass of the 128 threads
+  constexpr int NPASS = 128 / RPP;
+  constexpr int W = XB ? 4 : 8;              // 32-bit words per unit
+  constexpr int NBATCH = (XB || NCH == 1) ? 1 : 2;
+  constexpr int NB = NPASS / NBATCH;
+  const int ch = tid % UPR;
+  const int r0 = tid / UPR;
+  const int d0 = ch * 8;
+  const Meta* meta = a.meta;
+  float shift[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) shift[e] = d0 + e < a.D ? meta->shift[d0 + e] : 0.f;
+  const float scale = meta->scale;
+  const bool vec = (a.D % 8) == 0;
+  const bool unit_in = d0 < a.D;
+  uint32_t buf[NB][W];
+
+  auto load_batch = [&](int t, int b) {
+#pragma unroll
+    for (int p = 0; p < NB; ++p) {
+      const int row = r0 + RPP * (b * NB + p);
+      const int64_t n = static_cast<int64_t>(t) * kBN + row;
+#pragma unroll
+      for (int e = 0; e < W; ++e) buf[p][e] = 0u;
+      if (n < a.N && unit_in) {
+        if constexpr (XB) {
+          const uint16_t* xr = static_cast<const uint16_t*>(a.X) + n * a.D + d0;
+          if (vec) {
+            const uint4 v = ldg_stream_v4(xr);
+            buf[p][0] = v.x; buf[p][1] = v.y; buf[p][2] = v.z; buf[p][3] = v.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (d0 + e < a.D) buf[p][e >> 1] |= static_cast<uint32_t>(__ldg(xr + e)) << (16 * (e & 1));
+          }
+        } else {
+          const float* xr = static_cast<const float*>(a.X) + n * a.D + d0;
+          if (vec) {
+            const uint4 v0 = ldg_stream_v4(xr);
+            const uint4 v1 = ldg_stream_v4(xr + 4);
+            buf[p][0] = v0.x; buf[p][1] = v0.y; buf[p][2] = v0.z; buf[p][3] = v0.w;
+            buf[p][4] = v1.x; buf[p][5] = v1.y; buf[p][6] = v1.z; buf[p][7] = v1.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (d0 + e < a.D) buf[p][e] = __float_as_uint(__ldg(xr + e));
+          }
+        }
+      }
+    }
+  };
+
+  auto store_batch = [&](int t, int b, uint8_t* stage) {
+#pragma unroll
+    for (int p = 0; p < NB; ++p) {
+      const int row = r0 + RPP * (b * NB + p);
+      const bool valid = static_cast<int64_t>(t) * kBN + row < a.N;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float v;
+        if constexpr (XB) v = __uint_as_float((e & 1) ? (buf[p][e >> 1] & 0xffff0000u) : (buf[p][e >> 1] << 16));
+        else v = __uint_as_float(buf[p][e]);
+        x[e] = valid ? (v - shift[e]) * scale : 0.f;
+      }
+      const uint32_t off = (ch / 8) * kChunkBytes + sw128_off(row, ch % 8);
+      const uint32_t off2 = off + NCH * kChunkBytes;
+      if constexpr (NP == 1) {
+        uint4 hx, hq;
+        hx.x = pack_f16x2(x[0], x[1]); hx.y = pack_f16x2(x[2], x[3]);
+        hx.z = pack_f16x2(x[4], x[5]); hx.w = pack_f16x2(x[6], x[7]);
+        if (XB) {
+          // bf16 data scaled by a power of two are exact in fp16, so the
+          // fp16 square of the packed value rounds the exact x'^2 once
+          hq.x = sq_f16x2(hx.x); hq.y = sq_f16x2(hx.y); hq.z = sq_f16x2(hx.z); hq.w = sq_f16x2(hx.w);
+        } else {
+          hq.x = pack_f16x2(x[0] * x[0], x[1] * x[1]); hq.y = pack_f16x2(x[2] * x[2], x[3] * x[3]);
+          hq.z = pack_f16x2(x[4] * x[4], x[5] * x[5]); hq.w = pack_f16x2(x[6] * x[6], x[7] * x[7]);
+        }
+        *reinterpret_cast<uint4*>(stage + off) = hx;
+        *reinterpret_cast<uint4*>(stage + off2) = hq;
+      } else {
+        float xh[8], xl[8], qh[8], ql[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          xh[e] = __half2float(__float2half_rn(x[e]));
+          xl[e] = x[e] - xh[e];
+          const float q = x[e] * x[e];
+          qh[e] = __half2float(__float2half_rn(q));
+          ql[e] = q - qh[e];
+        }
+        uint4 v;
+        v.x = pack_f16x2(xh[0], xh[1]); v.y = pack_f16x2(xh[2], xh[3]);
+        v.z = pack_f16x2(xh[4], xh[5]); v.w = pack_f16x2(xh[6], xh[7]);
+        *reinterpret_cast<uint4*>(stage + off) = v;
+        v.x = pack_f16x2(qh[0], qh[1]); v.y = pack_f16x2(qh[2], qh[3]);
+        v.z = pack_f16x2(qh[4], qh[5]); v.w = pack_f16x2(qh[6], qh[7]);
+        *reinterpret_cast<uint4*>(stage + off2) = v;
+        v.x = pack_f16x2(xl[0], xl[1]); v.y = pack_f16x2(xl[2], xl[3]);
+        v.z = pack_f16x2(xl[4], xl[5]); v.w = pack_f16x2(xl[6], xl[7]);
+        *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off) = v;
+        v.x = pack_f16x2(ql[0], ql[1]); v.y = pack_f16x2(ql[2], ql[3]);
+        v.z = pack_f16x2(ql[4], ql[5]); v.w = pack_f16x2(ql[6], ql[7]);
+        *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off2) = v;
+      }
+    }
+  };
+
+  const int nst = a.mode == MODE_TOPM ? 1 : NST;
+  if (NBATCH == 1 && my_tiles > 0) load_batch(tgroup, 0);
+  int t = tgroup;
+#pragma unroll 1
+  for (int j = 0; j < my_tiles; ++j, t += n_tgroups) {
+    if ((j & 7) == 0 && bar_red_or(2, 128, *abort_flag != 0)) break;
+    const int s = j % nst, use = j / nst;
+    if (use > 0) mbar_wait(&S->empty_a[s], (use - 1) & 1, abort_flag, a.status);
+    uint8_t* stage = sm + CF::kOffA + s * CF::kStageBytes;
+#pragma unroll
+    for (int b = 0; b < NBATCH; ++b) {
+      if (NBATCH > 1) load_batch(t, b);
+      store_batch(t, b, stage);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(&S->full_a[s]);
+    if (NBATCH == 1 && j + 1 < my_tiles) load_batch(t + n_tgroups, 0);
+  }
+}
+
 // ============================================================== fused kernel
 template <int NP, int NCH, int NST>
-__global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
+__global__ void __maxnreg__(152) fused_em_kernel(const FusedArgs a) {
   using CF = Cfg<NP, NCH, NST>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -267,8 +580,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S->full_a[i], 128);
       mbar_init(&S->empty_a[i], 1);
-      mbar_init(&S->xready[i], C);
-      mbar_init(&S->xfree[i], C);
+      mbar_init(&S->xready[i], 1);
     }
     mbar_init(&S->p_full, 1);
     mbar_init(&S->acc1_full, 1);
@@ -278,6 +590,8 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     mbar_init(&S->acc2_full, 1);
     mbar_init(&S->acc2_empty, 256);
     mbar_init(&S->drain, 1);
+    mbar_init(&S->tready, C);
+    mbar_init(&S->tfree, C);
     fence_mbar_init();
   }
   if (warp == 12) {
@@ -291,13 +605,6 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       S->iscale[j] = a.iscale[kbase + j];
     }
   }
-  if (tid < 128) {
-    // the all-ones operand that turns the statistics MMA into a row count
-    const uint32_t one2 = 0x3C003C00u;   // pairs of fp16 1.0
-    uint32_t* ones = reinterpret_cast<uint32_t*>(sm + CF::kOffOnes);
-    for (int i = tid; i < 512; i += 128) ones[i] = one2;
-    fence_proxy_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   if (C > 1 && !given) cluster_sync();
@@ -309,102 +616,12 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
   const uint32_t sA = smem_u32(sm + CF::kOffA);
   const uint32_t sP = smem_u32(sm + CF::kOffP);
   const uint32_t sR = smem_u32(sm + CF::kOffR);
-  const uint32_t sOnes = smem_u32(sm + CF::kOffOnes);
   constexpr uint32_t kAbType = 0u;   // fp16 operands (PRECISE: hi and lo pieces)
 
   if (warp < 4) {
     // ================================================= transform warps
-    constexpr int UPR = 8 * NCH;                     // 8-element units per row
-    const int ch = tid % UPR;                        // fixed feature unit of this thread
-    const int d0 = ch * 8;
-    const Meta* meta = a.meta;
-    float shift[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) shift[e] = d0 + e < a.D ? meta->shift[d0 + e] : 0.f;
-    const float scale = meta->scale;
-    const bool vec = (a.D % 8) == 0;
-    int j = 0;
-    for (int t = tgroup; j < my_tiles; t += n_tgroups, ++j) {
-      if (bar_red_or(2, 128, *abort_flag != 0)) break;
-      const int s = j % NST, use = j / NST;
-      if (use > 0) mbar_wait(&S->empty_a[s], (use - 1) & 1, abort_flag, a.status);
-      uint8_t* stage = sm + CF::kOffA + s * CF::kStageBytes;
-#pragma unroll 1
-      for (int i = 0; i < 128 / (128 / UPR); ++i) {
-        const int u = tid + 128 * i;
-        const int row = u / UPR;
-        const int64_t n = static_cast<int64_t>(t) * kBN + row;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        if (n < a.N && d0 < a.D) {
-          if (a.x_bf16) {
-            const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(a.X) + n * a.D + d0;
-            if (vec) {
-              uint4 v = __ldg(reinterpret_cast<const uint4*>(xr));
-              uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                x[2 * e] = __uint_as_float(w[e] << 16);
-                x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] = d0 + e < a.D ? __bfloat162float(xr[e]) : 0.f;
-            }
-          } else {
-            const float* xr = static_cast<const float*>(a.X) + n * a.D + d0;
-            if (vec) {
-              float4 v0 = __ldg(reinterpret_cast<const float4*>(xr));
-              float4 v1 = __ldg(reinterpret_cast<const float4*>(xr) + 1);
-              x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
-              x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] = d0 + e < a.D ? xr[e] : 0.f;
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = d0 + e < a.D ? (x[e] - shift[e]) * scale : 0.f;
-        }
-        const uint32_t off = (ch / 8) * kChunkBytes + sw128_off(row, ch % 8);
-        const uint32_t off2 = off + NCH * kChunkBytes;
-        if constexpr (NP == 1) {
-          uint4 hx, hq;
-          hx.x = pack_f16x2(x[0], x[1]); hx.y = pack_f16x2(x[2], x[3]);
-          hx.z = pack_f16x2(x[4], x[5]); hx.w = pack_f16x2(x[6], x[7]);
-          hq.x = pack_f16x2(x[0] * x[0], x[1] * x[1]); hq.y = pack_f16x2(x[2] * x[2], x[3] * x[3]);
-          hq.z = pack_f16x2(x[4] * x[4], x[5] * x[5]); hq.w = pack_f16x2(x[6] * x[6], x[7] * x[7]);
-          *reinterpret_cast<uint4*>(stage + off) = hx;
-          *reinterpret_cast<uint4*>(stage + off2) = hq;
-        } else {
-          float xh[8], xl[8], qh[8], ql[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            xh[e] = __half2float(__float2half_rn(x[e]));
-            xl[e] = x[e] - xh[e];
-            const float q = x[e] * x[e];
-            qh[e] = __half2float(__float2half_rn(q));
-            ql[e] = q - qh[e];
-          }
-          uint4 v;
-          v.x = pack_f16x2(xh[0], xh[1]); v.y = pack_f16x2(xh[2], xh[3]);
-          v.z = pack_f16x2(xh[4], xh[5]); v.w = pack_f16x2(xh[6], xh[7]);
-          *reinterpret_cast<uint4*>(stage + off) = v;
-          v.x = pack_f16x2(qh[0], qh[1]); v.y = pack_f16x2(qh[2], qh[3]);
-          v.z = pack_f16x2(qh[4], qh[5]); v.w = pack_f16x2(qh[6], qh[7]);
-          *reinterpret_cast<uint4*>(stage + off2) = v;
-          v.x = pack_f16x2(xl[0], xl[1]); v.y = pack_f16x2(xl[2], xl[3]);
-          v.z = pack_f16x2(xl[4], xl[5]); v.w = pack_f16x2(xl[6], xl[7]);
-          *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off) = v;
-          v.x = pack_f16x2(ql[0], ql[1]); v.y = pack_f16x2(ql[2], ql[3]);
-          v.z = pack_f16x2(ql[4], ql[5]); v.w = pack_f16x2(ql[6], ql[7]);
-          *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off2) = v;
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&S->full_a[s]);
-    }
+    if (a.x_bf16) transform_warps<CF, NP, NCH, NST, true>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
+    else transform_warps<CF, NP, NCH, NST, false>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
   } else if (warp < 12) {
     // ================================================= softmax warps
     const int st = tid - 128;            // 0..255
@@ -414,10 +631,16 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     const int rho = q >> 1;              // statistics half this row belongs to
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     double ll = 0.0;
+    float llf = 0.f;              // fp32 part of ll, moved into ll at every flush
+    // the rows of a tile share the log-likelihood work among the CTAs of a cluster
+    const bool ll_row = h == 0 && (nl % C) == rank;
+    float s0a = 0.f, s0b = 0.f;   // S0 partials of two components (see column_sums_32)
     int flush_idx = 0;
     int j = 0;
     for (int t = tgroup; j < my_tiles; t += n_tgroups, ++j) {
-      if (bar_red_or(1, 256, *abort_flag != 0)) break;
+      // all 256 threads agree on stopping (waits return at once after an abort,
+      // so every thread reaches this check)
+      if ((j & 7) == 0 && bar_red_or(1, 256, *abort_flag != 0)) break;
       const int64_t n = static_cast<int64_t>(t) * kBN + nl;
       const bool valid = n < a.N;
       mbar_wait(&S->acc1_full, j & 1, abort_flag, a.status);
@@ -433,24 +656,34 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&S->acc1_empty);
-      // logits (log2 units) and the row maximum
+      // logits (log2 units) and the row maximum; padded and dead components
+      // have cadj = -inf (and a zero operand row), so their logit is -inf
       float m = -CUDART_INF_F;
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const int k = 64 * h + e;
-        const float l = k < kvalid ? fmaf(v[e], S->iscale[k], S->cadj[k]) : -CUDART_INF_F;
-        v[e] = l;
-        m = fmaxf(m, l);
+      for (int e4 = 0; e4 < 16; ++e4) {
+        const float4 sc = *reinterpret_cast<const float4*>(&S->iscale[64 * h + 4 * e4]);
+        const float4 cc = *reinterpret_cast<const float4*>(&S->cadj[64 * h + 4 * e4]);
+        v[4 * e4 + 0] = fmaf(v[4 * e4 + 0], sc.x, cc.x);
+        v[4 * e4 + 1] = fmaf(v[4 * e4 + 1], sc.y, cc.y);
+        v[4 * e4 + 2] = fmaf(v[4 * e4 + 2], sc.z, cc.z);
+        v[4 * e4 + 3] = fmaf(v[4 * e4 + 3], sc.w, cc.w);
+        m = fmaxf(fmaxf(m, fmaxf(v[4 * e4 + 0], v[4 * e4 + 1])), fmaxf(v[4 * e4 + 2], v[4 * e4 + 3]));
       }
       S->pair_m[h][nl] = m;
       named_bar_sync(1, 256);
       m = fmaxf(S->pair_m[0][nl], S->pair_m[1][nl]);
+      const float mh = S->pair_m[h][nl];   // maximum over this half (MODE_TOPM keys)
       float ssum = 0.f;
+      if (a.mode == MODE_TOPM) {
 #pragma unroll
-      for (int e = 0; e < 64; ++e) {
-        const float p = m == -CUDART_INF_F ? 0.f : ex2(v[e] - m);
-        v[e] = p;
-        ssum += p;
+        for (int e = 0; e < 64; ++e) ssum += m == -CUDART_INF_F ? 0.f : ex2(v[e] - m);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const float p = m == -CUDART_INF_F ? 0.f : ex2(v[e] - m);
+          v[e] = p;
+          ssum += p;
+        }
       }
       S->pair_s[h][nl] = ssum;
       named_bar_sync(1, 256);
@@ -460,39 +693,57 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       if (given) {
         lse = valid ? __ldg(a.lse_in + n) : -CUDART_INF_F;
       } else if (C > 1) {
-        const int slot = j & 1, use = j >> 1;
+        // Every CTA of the cluster pushes its row normalisers into slot j & 1 of
+        // every CTA (itself included); the slot's barrier completes when all
+        // C * 128 floats have landed.  Two slots suffice: a CTA pushes tile
+        // j + 2 only after every CTA has pushed tile j + 1, which each does
+        // only after all of its threads have read slot j & 1 for tile j.
+        const int slot = j & 1;
         if (h == 0) {
-          if (use > 0) mbar_wait(&S->xfree[slot], (use - 1) & 1, abort_flag, a.status);
-          S->xsend[slot][nl] = lse_loc;
-        }
-        named_bar_sync(1, 256);
-        if (st == 0) {
-          fence_acq_rel_cluster();
+          const uint32_t dst = smem_u32(&S->xrecv[slot][rank][nl]);
           const uint32_t bar = smem_u32(&S->xready[slot]);
-          for (int r = 0; r < C; ++r) mbar_arrive_remote(mapa(bar, r));
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            if (r < C) st_async_f32(mapa(dst, r), lse_loc, mapa(bar, r));
         }
-        mbar_wait_cluster(&S->xready[slot], use & 1, abort_flag, a.status);
-        const uint32_t src = smem_u32(&S->xsend[slot][nl]);
+        if (st == 0) mbar_arrive_expect_tx(&S->xready[slot], static_cast<uint32_t>(C * kBN * 4));
+        mbar_wait(&S->xready[slot], (j >> 1) & 1, abort_flag, a.status);
         float vals[8];
-        float mx = -CUDART_INF_F;
-        for (int r = 0; r < C; ++r) {
-          vals[r] = ld_cluster_f32(mapa(src, r));
-          mx = fmaxf(mx, vals[r]);
-        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) vals[r] = r < C ? S->xrecv[slot][r][nl] : -CUDART_INF_F;
+        float mx = vals[0];
+#pragma unroll
+        for (int r = 1; r < 8; ++r) mx = fmaxf(mx, vals[r]);
         float s2 = 0.f;
-        for (int r = 0; r < C; ++r) s2 += mx == -CUDART_INF_F ? 0.f : ex2(vals[r] - mx);
-        lse = s2 > 0.f ? mx + lg2(s2) : -CUDART_INF_F;
-        named_bar_sync(1, 256);
-        if (st == 0) {
-          const uint32_t bar = smem_u32(&S->xfree[slot]);
-          for (int r = 0; r < C; ++r) mbar_arrive_remote(mapa(bar, r));
+        if (mx > -CUDART_INF_F) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) s2 += ex2(vals[r] - mx);
         }
+        lse = s2 > 0.f ? mx + lg2(s2) : -CUDART_INF_F;
       }
       if (a.mode == MODE_LSE) {
         if (rank == 0 && h == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
         continue;
       }
-      if (a.mode == MODE_EM && rank == 0 && h == 0 && valid) ll += static_cast<double>(lse);
+      if (a.mode == MODE_TOPM) {
+        if (a.topm_groups > 1) {
+          if (rank == 0 && h == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
+        } else if (ll_row && valid) {
+          llf += lse;
+        }
+        // candidate lists: the second data stage (unused in this mode), or the
+        // R tile area of the single-stage configuration
+        uint8_t* lists = NST == 2 ? sm + CF::kOffA + CF::kStageBytes : sm + CF::kOffR;
+        const int64_t n0 = static_cast<int64_t>(t) * kBN;
+        switch (a.topm_max) {
+          case 2: topm_tile<2>(a, S, lists, v, mh, lse, n0, nl, h, lane, warp, st, rank, C, kbase, j, abort_flag); break;
+          case 4: topm_tile<4>(a, S, lists, v, mh, lse, n0, nl, h, lane, warp, st, rank, C, kbase, j, abort_flag); break;
+          case 8: topm_tile<8>(a, S, lists, v, mh, lse, n0, nl, h, lane, warp, st, rank, C, kbase, j, abort_flag); break;
+          default: topm_tile<16>(a, S, lists, v, mh, lse, n0, nl, h, lane, warp, st, rank, C, kbase, j, abort_flag); break;
+        }
+        continue;
+      }
+      if (a.mode == MODE_EM && ll_row && valid) llf += lse;
       // r is stored as r * 2^15 in fp16 so that small responsibilities stay
       // out of the fp16 subnormal range; finalize divides the statistics back.
       const float rscale = 32768.f;
@@ -503,10 +754,10 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       const int nr = nl - 64 * rho;        // row inside the 64-point half
       uint8_t* rbase = sm + CF::kOffR + h * 8192;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float r8[8];
+      for (int e = 0; e < 64; ++e) v[e] *= f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) r8[e] = v[8 * c + e] * f;
+      for (int c = 0; c < 8; ++c) {
+        const float* r8 = v + 8 * c;
         const uint32_t off = sw128_off(nr, c);
         if constexpr (NP == 1) {
           uint4 w;
@@ -531,9 +782,25 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       }
       fence_proxy_async_smem();
       mbar_arrive(&S->r_full);
+      // S0: column sums of r over the 32 points (lanes) of this warp; lane l
+      // ends with components 64h + 2l and 64h + 2l + 1, kept across tiles
+      column_sums_32(v, lane);
+      s0a += v[0];
+      s0b += v[1];
       // statistics leave tensor memory at the end of a flush period
       const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
       if (flush && stats) {
+        // S0 partials of the four lane quarters meet in shared memory (the
+        // pair arrays are free here)
+        float* s0red = &S->pair_m[0][0];       // [4][128] over pair_m and pair_s
+        named_bar_sync(1, 256);                 // every read of pair_s of this tile is done
+        s0red[q * 128 + 64 * h + 2 * lane] = s0a;
+        s0red[q * 128 + 64 * h + 2 * lane + 1] = s0b;
+        s0a = 0.f;
+        s0b = 0.f;
+        ll += static_cast<double>(llf);
+        llf = 0.f;
+        named_bar_sync(1, 256);
         mbar_wait(&S->acc2_full, flush_idx & 1, abort_flag, a.status);
         tc_fence_after();
         // lanes = components 32q + lane; h = 0: S1 and S0, h = 1: S2
@@ -549,26 +816,27 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
             for (int e = 0; e < 16; ++e) prow[c0 + c + e] += static_cast<double>(w[e]);
           }
         }
-        if (h == 0) {
-          float w[16];
-          tmem_ld16(acc2 + lane_off + 2 * CF::kDp, w);
-          tmem_wait_ld();
-          if (kl < kvalid) prow[2 * CF::kDp] += static_cast<double>(w[0]);
+        if (h == 0 && kl < kvalid) {
+          const float t0 = s0red[kl] + s0red[128 + kl];
+          const float t1 = s0red[256 + kl] + s0red[384 + kl];
+          prow[2 * CF::kDp] += static_cast<double>(t0) + static_cast<double>(t1);
         }
         tc_fence_before();
         mbar_arrive(&S->acc2_empty);
         ++flush_idx;
+        named_bar_sync(1, 256);    // s0red is read before the pair arrays are reused
       }
     }
     // log-likelihood partial of this cluster (rank 0 only)
-    if (a.mode == MODE_EM) {
+    if (a.mode == MODE_EM || (a.mode == MODE_TOPM && a.topm_groups == 1)) {
+      ll += static_cast<double>(llf);
       for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, o);
       if (lane == 0) S->ll_red[warp - 4] = ll;
       named_bar_sync(1, 256);
-      if (st == 0 && rank == 0) {
+      if (st == 0) {
         double tot = 0.0;
         for (int i = 0; i < 8; ++i) tot += S->ll_red[i];
-        a.ll_part[tgroup] = tot * kLn2;
+        a.ll_part[tgroup * C + rank] = tot * kLn2;
       }
     }
   } else {
@@ -584,12 +852,12 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
 
       const uint32_t id1 = idesc_f16(kAbType, 0, 0, 128, n1);
       const uint32_t id2 = idesc_f16(kAbType, 1, 1, 128, 2 * CF::kDp);
-      const uint32_t id0 = idesc_f16(kAbType, 1, 1, 128, 16);
       int flush_idx = 0;
       bool fresh = true;   // next statistics MMA starts a new accumulation
+      const int nst = a.mode == MODE_TOPM ? 1 : NST;   // MODE_TOPM: stage 1 holds the lists
 
       auto issue_g1 = [&](int jj) {
-        const int s = jj % NST;
+        const int s = jj % nst;
         const uint32_t stage = sA + s * CF::kStageBytes;
         uint32_t accf = 0;
 #pragma unroll
@@ -607,7 +875,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
         mma_commit(&S->acc1_full);
       };
       auto wait_a = [&](int jj) {
-        mbar_wait(&S->full_a[jj % NST], (jj / NST) & 1, abort_flag, a.status);
+        mbar_wait(&S->full_a[jj % nst], (jj / nst) & 1, abort_flag, a.status);
         tc_fence_after();
       };
 
@@ -626,7 +894,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
             mbar_wait(&S->acc1_empty, j & 1, abort_flag, a.status);
             tc_fence_after();
             issue_g1(j + 1);
-            if (!stats) mma_commit(&S->empty_a[(j + 1) % NST]);
+            if (!stats) mma_commit(&S->empty_a[(j + 1) % nst]);
           }
         }
         if (stats) {
@@ -650,15 +918,6 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
                 fresh = false;
               }
             }
-            // S0: responsibilities against an all-ones operand
-            bool fresh0 = (rho == 0) && (j == 0 || ((j) % a.flush_tiles == 0));
-            for (int prr = 0; prr < NP; ++prr)
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = sdesc_sw128(sR + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
-                const uint64_t bd = sdesc_sw128(sOnes, kChunkBytes, 1024);
-                mma_f16_ss(acc2 + 2 * CF::kDp, ad, bd, id0, fresh0 ? 0u : 1u);
-                fresh0 = false;
-              }
             mma_commit(&S->r_empty);
           }
           mma_commit(&S->empty_a[s]);
@@ -716,6 +975,77 @@ __global__ void lse_combine_kernel(const float* __restrict__ lse_part, int n_gro
     double t = 0.0;
     for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += red[i];
     ll_part[blockIdx.x] = t * kLn2;
+  }
+}
+
+// ============================================================== top-m combine (K > 1024)
+// Per point: the normaliser over all K groups and the best m of the groups'
+// candidate lists (each sorted, best first); ties go to the lower index.
+__global__ void topm_combine_kernel(const float* __restrict__ lse_part, const float* __restrict__ gval,
+                                    const int32_t* __restrict__ gidx, int n_groups, int64_t N, int m,
+                                    float* __restrict__ resp_out, int32_t* __restrict__ idx_out,
+                                    double* __restrict__ ll_part) {
+  __shared__ double red[8];
+  double acc = 0.0;
+  for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < N;
+       n += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float mx = -CUDART_INF_F;
+    for (int g = 0; g < n_groups; ++g) mx = fmaxf(mx, lse_part[static_cast<int64_t>(g) * N + n]);
+    float s = 0.f;
+    if (mx > -CUDART_INF_F)
+      for (int g = 0; g < n_groups; ++g) s += ex2(lse_part[static_cast<int64_t>(g) * N + n] - mx);
+    const float lse = s > 0.f ? mx + lg2(s) : -CUDART_INF_F;
+    acc += static_cast<double>(lse);
+    float bv[16];
+    int32_t bi[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      bv[u] = -CUDART_INF_F;
+      bi[u] = 0x7fffffff;
+    }
+    for (int g = 0; g < n_groups; ++g) {
+      const int64_t base = (static_cast<int64_t>(g) * N + n) * m;
+      for (int c = 0; c < m; ++c) {
+        float cv = gval[base + c];
+        int32_t ci = gidx[base + c];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const bool better = cv > bv[u] || (cv == bv[u] && ci < bi[u]);
+          const float tv = better ? bv[u] : cv;
+          const int32_t ti = better ? bi[u] : ci;
+          if (better) {
+            bv[u] = cv;
+            bi[u] = ci;
+          }
+          cv = tv;
+          ci = ti;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      if (u < m) {
+        resp_out[n * m + u] = lse > -CUDART_INF_F ? ex2(bv[u] - lse) : 0.f;
+        idx_out[n * m + u] = bi[u];
+      }
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += red[i];
+    ll_part[blockIdx.x] = t * kLn2;
+  }
+}
+
+// Sum of n partial log-likelihoods in a fixed order (one thread).
+__global__ void ll_total_kernel(const double* __restrict__ parts, int n, double* __restrict__ out) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < n; ++i) t += parts[i];
+    *out = t;
   }
 }
 
@@ -797,6 +1127,8 @@ const void* kernel_handle(KernelId id) {
     case K_FUSED_2_1_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 1, 1>);
     case K_LSE_COMBINE: return reinterpret_cast<const void*>(&lse_combine_kernel);
     case K_FINALIZE: return reinterpret_cast<const void*>(&finalize_kernel);
+    case K_TOPM_COMBINE: return reinterpret_cast<const void*>(&topm_combine_kernel);
+    case K_LL_TOTAL: return reinterpret_cast<const void*>(&ll_total_kernel);
   }
   return nullptr;
 }

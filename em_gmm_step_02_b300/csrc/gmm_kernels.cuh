@@ -27,6 +27,7 @@ struct Meta {
 enum KernelId : int {
   K_ABSMAX, K_ABSMAX_VEC, K_META, K_PARAMS_FAST, K_PARAMS_PRECISE,
   K_FUSED_1_1_2, K_FUSED_1_2_2, K_FUSED_2_1_1, K_LSE_COMBINE, K_FINALIZE,
+  K_TOPM_COMBINE, K_LL_TOTAL,
 };
 
 // Host-side handle of a kernel, for cudaLaunchKernelEx (argument order and
@@ -53,6 +54,7 @@ struct FusedArgs {
   int flush_tiles;     // statistics leave tensor memory every this many tiles
   int F;               // doubles per component row of the partial statistics
   int topm;            // m of the top-m mode
+  int topm_max;        // m rounded up to a power of two (2..16): candidate list length
   const uint8_t* p_img;   // parameter operand images, one per slice
   const float* cadj;      // per-component logit constant (log2 units)
   const float* iscale;    // per-component scale of the logit accumulator
@@ -61,28 +63,11 @@ struct FusedArgs {
   double* ll_part;        // per tile group log-likelihood partials
   float* lse_part;        // MODE_LSE output [K group][N] (log2 units)
   const float* lse_in;    // MODE_GIVEN input [N] (log2 units)
-  float* topm_val;        // MODE_TOPM output values [K group][N][m] (log2 logits)
-  int32_t* topm_idx;      // MODE_TOPM output indices
+  float* topm_val;        // MODE_TOPM output: responsibilities [N][m] (one K group), or
+                          // per-group log2 logits [K group][N][m] (several K groups)
+  int32_t* topm_idx;      // MODE_TOPM output component indices, same layout
+  int topm_groups;        // number of K groups (gridDim.y); 1: final output
   uint32_t* status;
-};
-
-// Shared-memory plan of the fused kernel for NP operand pieces (1: fp16,
-// 2: bf16 hi/lo), NCH 64-feature atom columns per data part, NST data stages.
-template <int NP, int NCH, int NST>
-struct Cfg {
-  static constexpr int kPieceBytes = 2 * NCH * kChunkBytes;          // [x | x^2] for 128 rows
-  static constexpr int kStageBytes = NP * kPieceBytes;
-  static constexpr int kOffA = 0;
-  static constexpr int kOffP = NST * kStageBytes;
-  static constexpr int kOffR = kOffP + NP * kPieceBytes;
-  static constexpr int kRBytes = 64 * kSlice * 2;                     // 64 points x 128 comps x 16 bit
-  static constexpr int kOffOnes = kOffR + NP * kRBytes;
-  static constexpr int kOffSmall = kOffOnes + 2048;
-  static constexpr int kDp = NCH * kAtomElems;
-  static constexpr int kF2 = 2 * kDp + 16;                            // statistics columns in TMEM
-  static constexpr uint32_t kAcc1Col = 0;
-  static constexpr uint32_t kAcc2Col = 128;
-  static constexpr int kThreads = 13 * 32;
 };
 
 struct Small {
@@ -90,7 +75,8 @@ struct Small {
   float iscale[kSlice];
   float pair_m[2][kBN];
   float pair_s[2][kBN];
-  float xsend[2][kBN];
+  float xrecv[2][8][kBN];  // row normalisers pushed by each CTA of the cluster, per slot
+  float lse_row[kBN];     // MODE_TOPM: normaliser of each row of the tile (log2 units)
   double ll_red[8];
   uint64_t full_a[2];
   uint64_t empty_a[2];
@@ -101,11 +87,39 @@ struct Small {
   uint64_t r_empty;
   uint64_t acc2_full;
   uint64_t acc2_empty;
-  uint64_t xready[2];
-  uint64_t xfree[2];
+  uint64_t xready[2];     // slot filled: every CTA of the cluster has pushed its row normalisers
+  uint64_t tready;        // MODE_TOPM: candidate lists of every CTA of the cluster written
+  uint64_t tfree;         // MODE_TOPM: candidate lists of every CTA of the cluster consumed
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+
+// Shared-memory plan of the fused kernel for NP operand pieces (1: fp16,
+// 2: fp16 hi/lo), NCH 64-feature atom columns per data part, NST data stages:
+//   [data stages | parameter image | Small | R tile]
+// MODE_TOPM runs with one data stage; the second stage (or, with a single
+// stage, the R tile area) holds the per-row candidate lists.
+template <int NP, int NCH, int NST>
+struct Cfg {
+  static constexpr int kPieceBytes = 2 * NCH * kChunkBytes;          // [x | x^2] for 128 rows
+  static constexpr int kStageBytes = NP * kPieceBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffP = NST * kStageBytes;
+  static constexpr int kOffSmall = kOffP + NP * kPieceBytes;
+  static constexpr int kOffR = (kOffSmall + static_cast<int>(sizeof(Small)) + 1023) / 1024 * 1024;
+  static constexpr int kRBytes = 64 * kSlice * 2;                     // 64 points x 128 comps x 16 bit
+  static constexpr int kEnd = kOffR + NP * kRBytes;
+  static constexpr int kDp = NCH * kAtomElems;
+  static constexpr int kF2 = 2 * kDp;                                 // statistics columns in TMEM
+  static constexpr uint32_t kAcc1Col = 0;
+  static constexpr uint32_t kAcc2Col = 128;
+  static constexpr int kThreads = 13 * 32;
+};
+
+// MODE_TOPM candidate lists: for each of the 128 rows of a tile and each of
+// the two column halves, the MAXM best (logit, component) pairs (at most
+// 24 KB, within one data stage or the R tile area of every configuration).
+__host__ __device__ constexpr int topm_list_bytes(int maxm) { return kBN * 2 * maxm * 6; }
 
 }  // namespace gmm

@@ -40,6 +40,12 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_cluster_u16(uint32_t caddr) {
+  unsigned short v;
+  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(caddr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void ld_cluster_v2(uint32_t caddr, float& a, float& b) {
   asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(a), "=f"(b) : "r"(caddr) : "memory");
 }
@@ -126,6 +132,14 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   *abort = 1u;
   atomicOr(status, ST_TIMEOUT);
   return false;
+}
+
+// Store one float into shared memory of CTA-in-cluster address `caddr` and
+// signal 4 transaction bytes on the mbarrier at cluster address `cbar` (in
+// the same CTA as caddr).
+__device__ __forceinline__ void st_async_f32(uint32_t caddr, float v, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               :: "r"(caddr), "r"(__float_as_uint(v)), "r"(cbar) : "memory");
 }
 
 // ---------------------------------------------------------------- proxies
