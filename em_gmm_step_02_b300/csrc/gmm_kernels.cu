@@ -542,7 +542,7 @@ __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm,
 
 // ============================================================== fused kernel
 template <int NP, int NCH, int NST>
-__global__ void __maxnreg__(152) fused_em_kernel(const FusedArgs a) {
+__global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
   using CF = Cfg<NP, NCH, NST>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
