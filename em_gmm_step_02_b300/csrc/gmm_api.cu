@@ -92,10 +92,10 @@ size_t fused_smem(int np, int nch, int nst) {
   return std::max<size_t>(b, 120 * 1024);   // one CTA per SM: it owns all of tensor memory
 }
 
-const void* fused_fn(int np, int nch, int nst) {
-  if (np == 1 && nch == 1 && nst == 2) return kernel_handle(K_FUSED_1_1_2);
-  if (np == 1 && nch == 2 && nst == 2) return kernel_handle(K_FUSED_1_2_2);
-  if (np == 2 && nch == 1 && nst == 1) return kernel_handle(K_FUSED_2_1_1);
+const void* fused_fn(int np, int nch, int nst, bool topm = false) {
+  if (np == 1 && nch == 1 && nst == 2) return kernel_handle(topm ? K_TOPM_1_1_2 : K_FUSED_1_1_2);
+  if (np == 1 && nch == 2 && nst == 2) return kernel_handle(topm ? K_TOPM_1_2_2 : K_FUSED_1_2_2);
+  if (np == 2 && nch == 1 && nst == 1) return kernel_handle(topm ? K_TOPM_2_1_1 : K_FUSED_2_1_1);
   return nullptr;
 }
 
@@ -455,7 +455,7 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
     int Dp = p.nch * kAtomElems;
     if ((r = launch(kernel_handle(K_FINALIZE), dim3(p.K), dim3(128), 0, s, 1,
                     static_cast<const double*>(a.part), p.tg, p.K_pad, p.F, Dp, p.D, p.K, p.N, p.cov_diag, reg,
-                    floor_, 32768.0, static_cast<const Meta*>(a.meta), reinterpret_cast<const double*>(ws + p.off_llpart),
+                    floor_, static_cast<double>(p.fast ? kRScale<1>() : kRScale<2>()), static_cast<const Meta*>(a.meta), reinterpret_cast<const double*>(ws + p.off_llpart),
                     n_ll, new_log_weights, new_means, new_vars, means, vars, ll_dev)))
       return r;
   }
@@ -501,7 +501,7 @@ int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = nullptr;
   if ((r = get_workspace(need, &ws))) return r;
-  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  const void* fn = fused_fn(p.np, p.nch, p.nst, true);
   if ((r = set_smem_attr(fn, smem))) return r;
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
 
@@ -712,7 +712,7 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
     int Dp = p.nch * kAtomElems;
     if ((r = launch(kernel_handle(K_FINALIZE), dim3(p.K), dim3(128), 0, s, 1,
                     static_cast<const double*>(a.part), p.tg, p.K_pad, p.F, Dp, p.D, p.K, p.N, p.cov_diag, reg,
-                    floor_, 32768.0, static_cast<const Meta*>(a.meta),
+                    floor_, static_cast<double>(p.fast ? kRScale<1>() : kRScale<2>()), static_cast<const Meta*>(a.meta),
                     reinterpret_cast<const double*>(ws + p.off_llpart), p.tg * p.C, new_log_weights, new_means,
                     new_vars, means, vars, ll_dev)))
       return r;

@@ -65,6 +65,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ void red_add_f64(double* p, double v) {
+  asm volatile("red.global.add.f64 [%0], %1;" :: "l"(p), "d"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t sq_f16x2(uint32_t x) {
   __half2 h = *reinterpret_cast<__half2*>(&x);
   h = __hmul2(h, h);
@@ -368,30 +372,6 @@ __device__ __forceinline__ void topm_tile(const FusedArgs& a, Small* S, uint8_t*
   }
 }
 
-// ============================================================== column sums
-// Sums v[0..63] over the 32 lanes of the warp, column by column, with a
-// halving butterfly: at each step a lane keeps one half of its columns and
-// receives its partner's values for them.  On return v[0] and v[1] of lane l
-// hold the sums of columns 2l and 2l + 1; the rest of v is overwritten.
-template <int L, int O>
-__device__ __forceinline__ void bfly_step(float (&v)[64], int lane) {
-  const bool up = (lane & O) != 0;
-#pragma unroll
-  for (int i = 0; i < L / 2; ++i) {
-    const float send = up ? v[i] : v[i + L / 2];
-    const float keep = up ? v[i + L / 2] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-  }
-}
-
-__device__ __forceinline__ void column_sums_32(float (&v)[64], int lane) {
-  bfly_step<64, 16>(v, lane);
-  bfly_step<32, 8>(v, lane);
-  bfly_step<16, 4>(v, lane);
-  bfly_step<8, 2>(v, lane);
-  bfly_step<4, 1>(v, lane);
-}
-
 // ============================================================== data transform
 // 16-byte load that bypasses L1 (each data tile is read once per SM).
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
@@ -407,7 +387,7 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
 // Thread `tid` owns one 8-feature unit of every RPP-th row.  All loads of a
 // tile are issued together (and, when the registers allow, one tile ahead)
 // so that the whole tile is in flight at once.
-template <typename CF, int NP, int NCH, int NST, bool XB>
+template <typename CF, int NP, int NCH, int NST, bool XB, bool kTopm>
 __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm, Small* S,
                                                 volatile uint32_t* abort_flag, int tid, int tgroup,
                                                 int n_tgroups, int my_tiles) {
@@ -421,10 +401,10 @@ __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm,
   const int r0 = tid / UPR;
   const int d0 = ch * 8;
   const Meta* meta = a.meta;
-  float shift[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) shift[e] = d0 + e < a.D ? meta->shift[d0 + e] : 0.f;
   const float scale = meta->scale;
+  float nshift[8];                           // -shift * scale
+#pragma unroll
+  for (int e = 0; e < 8; ++e) nshift[e] = d0 + e < a.D ? -meta->shift[d0 + e] * scale : 0.f;
   const bool vec = (a.D % 8) == 0;
   const bool unit_in = d0 < a.D;
   uint32_t buf[NB][W];
@@ -464,10 +444,15 @@ __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm,
     }
   };
 
-  auto store_batch = [&](int t, int b, uint8_t* stage) {
+  auto store_batch = [&](int t, int b, uint8_t* stage, int s, int use) {
 #pragma unroll
     for (int p = 0; p < NB; ++p) {
-      const int row = r0 + RPP * (b * NB + p);
+      const int i = b * NB + p;
+      const int row = r0 + RPP * i;
+      // rows 16g..16g+15 of the stage are free once the statistics MMA of the
+      // stage's previous tile has consumed them
+      if ((RPP * i) % 16 == 0 && use > 0)
+        mbar_wait(&S->empty_g[s][(RPP * i) / 16], (use - 1) & 1, abort_flag, a.status);
       const bool valid = static_cast<int64_t>(t) * kBN + row < a.N;
       float x[8];
 #pragma unroll
@@ -475,7 +460,10 @@ __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm,
         float v;
         if constexpr (XB) v = __uint_as_float((e & 1) ? (buf[p][e >> 1] & 0xffff0000u) : (buf[p][e >> 1] << 16));
         else v = __uint_as_float(buf[p][e]);
-        x[e] = valid ? (v - shift[e]) * scale : 0.f;
+        // bf16 data in FAST are never shifted, and rows beyond N were loaded as
+        // zeros, so the plain scaling already leaves those rows zero
+        if constexpr (XB && NP == 1) x[e] = v * scale;
+        else x[e] = valid ? fmaf(v, scale, nshift[e]) : 0.f;
       }
       const uint32_t off = (ch / 8) * kChunkBytes + sw128_off(row, ch % 8);
       const uint32_t off2 = off + NCH * kChunkBytes;
@@ -520,19 +508,19 @@ __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm,
     }
   };
 
-  const int nst = a.mode == MODE_TOPM ? 1 : NST;
+  const int nst = kTopm ? 1 : NST;
   if (NBATCH == 1 && my_tiles > 0) load_batch(tgroup, 0);
   int t = tgroup;
 #pragma unroll 1
   for (int j = 0; j < my_tiles; ++j, t += n_tgroups) {
-    if ((j & 7) == 0 && bar_red_or(2, 128, *abort_flag != 0)) break;
+    // (no early exit on an abort: every wait below returns at once after one,
+    // so the loop runs out quickly and every barrier still sees all its threads)
     const int s = j % nst, use = j / nst;
-    if (use > 0) mbar_wait(&S->empty_a[s], (use - 1) & 1, abort_flag, a.status);
     uint8_t* stage = sm + CF::kOffA + s * CF::kStageBytes;
 #pragma unroll
     for (int b = 0; b < NBATCH; ++b) {
       if (NBATCH > 1) load_batch(t, b);
-      store_batch(t, b, stage);
+      store_batch(t, b, stage, s, use);
     }
     fence_proxy_async_smem();
     mbar_arrive(&S->full_a[s]);
@@ -540,8 +528,218 @@ __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm,
   }
 }
 
+// Adds this thread's row of the statistics accumulator (tensor-memory lane =
+// component; h = 0: S1 and S0, h = 1: S2) to its fp64 partial row.  Each
+// element of the partials has one writer, so fire-and-forget fp64 reductions
+// keep a fixed order of additions.
+template <int DP>
+__device__ __forceinline__ void flush_stats(double* prow, uint32_t taddr, int h, bool live) {
+  const int c0 = h == 0 ? 0 : DP;
+  for (int c = 0; c < DP; c += 16) {
+    float w[16];
+    tmem_ld16(taddr + c0 + c, w);
+    tmem_wait_ld();
+    if (live) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) red_add_f64(prow + c0 + c + e, static_cast<double>(w[e]));
+    }
+  }
+  if (h == 0) {
+    float w[16];
+    tmem_ld16(taddr + 2 * DP, w);
+    tmem_wait_ld();
+    if (live) red_add_f64(prow + 2 * DP, static_cast<double>(w[0]));
+  }
+}
+
+// ============================================================== FAST softmax warps
+// The softmax warps of the FAST (single fp16 piece) EM, normaliser and
+// statistics-given modes.  Per tile:
+//   A(j): logits of tile j from tensor memory (released at once), row
+//         maximum and sum over this CTA's 128 components, p = 2^(l - m + 10)
+//         kept as packed fp16 pairs, and this CTA's row normaliser, pushed
+//         to every CTA of the cluster.
+//   B(j): the row normaliser over the whole cluster (or read from memory),
+//         r * 2^10 = p * 2^(m - lse) by a packed multiply, the R tile for
+//         the statistics MMA, and the periodic flush of the statistics.
+// Two receive slots are safe: a CTA pushes tile t only after its B(t-1),
+// which needs every CTA's push of t-1, which each makes only after its own
+// B(t-2) has read the slot that tile t reuses.
+// The two warps that share a lane quarter (one per column half) meet at a
+// named barrier of their own.
+template <typename CF>
+__device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Small* S,
+                                             volatile uint32_t* abort_flag, int tid, int warp, int lane,
+                                             int rank, int C, int tgroup, int n_tgroups, int my_tiles,
+                                             uint32_t acc1, uint32_t acc2, int kbase, int kvalid) {
+  const int st = tid - 128;
+  const int q = warp & 3;                 // TMEM lane quarter
+  const int h = (warp - 4) >> 2;          // column half
+  const int nl = 32 * q + lane;           // point row inside the tile
+  const int rho = q >> 1;                 // statistics half this row belongs to
+  const int pbar = 3 + q;                 // named barrier of the pair of warps of this quarter
+  const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+  const bool given = a.mode == MODE_GIVEN;
+  const bool want_r = a.mode != MODE_LSE;
+  const bool exch = C > 1 && !given;
+  constexpr float kLog2R = 10.f;          // log2 of kRScale<1>()
+  double ll = 0.0;
+  float llf = 0.f;                        // fp32 part of ll, moved into ll at every flush
+  const bool ll_row = h == 0 && (nl % C) == rank;   // rows shared among the CTAs of a cluster
+  int flush_idx = 0;
+  for (int j = 0; j < my_tiles; ++j) {
+    // (no early exit on an abort: every wait returns at once after one, so the
+    // loop runs out quickly and both warps of a pair meet at every barrier)
+    // ---------------------------------------------------------------- A(j): local softmax
+    float v[64];
+    float m;
+    {
+      mbar_wait(&S->acc1_full, j & 1, abort_flag, a.status);
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float w[16];
+        tmem_ld16(acc1 + lane_off + 64 * h + 16 * c, w);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[16 * c + e] = w[e];
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&S->acc1_empty);
+      // logits (log2 units); padded and dead components have cadj = -inf
+      float mq[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+      for (int e4 = 0; e4 < 16; ++e4) {
+        const float4 sc = *reinterpret_cast<const float4*>(&S->iscale[64 * h + 4 * e4]);
+        const float4 cc = *reinterpret_cast<const float4*>(&S->cadj[64 * h + 4 * e4]);
+        v[4 * e4 + 0] = fmaf(v[4 * e4 + 0], sc.x, cc.x);
+        v[4 * e4 + 1] = fmaf(v[4 * e4 + 1], sc.y, cc.y);
+        v[4 * e4 + 2] = fmaf(v[4 * e4 + 2], sc.z, cc.z);
+        v[4 * e4 + 3] = fmaf(v[4 * e4 + 3], sc.w, cc.w);
+        mq[0] = fmaxf(mq[0], v[4 * e4 + 0]);
+        mq[1] = fmaxf(mq[1], v[4 * e4 + 1]);
+        mq[2] = fmaxf(mq[2], v[4 * e4 + 2]);
+        mq[3] = fmaxf(mq[3], v[4 * e4 + 3]);
+      }
+      S->pair_m[h][nl] = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      named_bar_sync(pbar, 64);
+      m = fmaxf(S->pair_m[0][nl], S->pair_m[1][nl]);
+    }
+    uint32_t pk[32];                      // p = 2^(l - m + 10), packed fp16 pairs
+    float lse_loc;
+    {
+      float sq[4] = {0.f, 0.f, 0.f, 0.f};
+      if (m > -CUDART_INF_F) {
+        const float mo = m - kLog2R;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(v[2 * i] - mo);
+          const float p1 = ex2(v[2 * i + 1] - mo);
+          sq[i & 3] += p0 + p1;
+          pk[i] = pack_f16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+      }
+      S->pair_s[h][nl] = (sq[0] + sq[1]) + (sq[2] + sq[3]);
+      named_bar_sync(pbar, 64);
+      const float tot = S->pair_s[0][nl] + S->pair_s[1][nl];
+      lse_loc = tot > 0.f ? m + lg2(tot) - kLog2R : -CUDART_INF_F;
+    }
+    // push this CTA's row normalisers of tile j to every CTA of the cluster
+    if (exch && h == 0) {
+      const uint32_t dst = smem_u32(&S->xrecv[j & 1][rank][nl]);
+      const uint32_t bar = smem_u32(&S->xready[j & 1]);
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < C) st_async_f32(mapa(dst, r), lse_loc, mapa(bar, r));
+    }
+    // ---------------------------------------------------------------- B(j): normalise, R tile
+    const int64_t pn = static_cast<int64_t>(tgroup + j * n_tgroups) * kBN + nl;
+    const float pm = m;
+    const float plse = lse_loc;
+    {
+      const int jj = j;
+      const bool valid = pn < a.N;
+      float lse = plse;
+      if (given) {
+        lse = valid ? __ldg(a.lse_in + pn) : -CUDART_INF_F;
+      } else if (C > 1) {
+        const int slot = jj & 1;
+        if (st == 0) mbar_arrive_expect_tx(&S->xready[slot], static_cast<uint32_t>(C * kBN * 4));
+        mbar_wait(&S->xready[slot], (jj >> 1) & 1, abort_flag, a.status);
+        float vals[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) vals[r] = r < C ? S->xrecv[slot][r][nl] : -CUDART_INF_F;
+        float mx = vals[0];
+#pragma unroll
+        for (int r = 1; r < 8; ++r) mx = fmaxf(mx, vals[r]);
+        float s2 = 0.f;
+        if (mx > -CUDART_INF_F) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) s2 += ex2(vals[r] - mx);
+        }
+        lse = s2 > 0.f ? mx + lg2(s2) : -CUDART_INF_F;
+      }
+      if (!want_r) {
+        if (rank == 0 && h == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + pn] = lse;
+      } else {
+        if (a.mode == MODE_EM && ll_row && valid) llf += lse;
+        const float f = (valid && lse > -CUDART_INF_F && pm > -CUDART_INF_F) ? ex2(pm - lse) : 0.f;
+        const __half2 f2 = __float2half2_rn(f);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          __half2 x = *reinterpret_cast<__half2*>(&pk[i]);
+          x = __hmul2(x, f2);
+          pk[i] = *reinterpret_cast<uint32_t*>(&x);
+        }
+        const int ru = 2 * jj + rho;      // use index of the R buffer
+        if (ru > 0) mbar_wait(&S->r_empty, (ru - 1) & 1, abort_flag, a.status);
+        uint8_t* rbase = sm + CF::kOffR + h * 8192;
+        const int nr = nl - 64 * rho;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 w;
+          w.x = pk[4 * c]; w.y = pk[4 * c + 1]; w.z = pk[4 * c + 2]; w.w = pk[4 * c + 3];
+          *reinterpret_cast<uint4*>(rbase + sw128_off(nr, c)) = w;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&S->r_full);
+        // statistics leave tensor memory at the end of a flush period
+        if (((jj + 1) % a.flush_tiles == 0) || (jj + 1 == my_tiles)) {
+          ll += static_cast<double>(llf);
+          llf = 0.f;
+          mbar_wait(&S->acc2_full, flush_idx & 1, abort_flag, a.status);
+          tc_fence_after();
+          flush_stats<CF::kDp>(a.part + (static_cast<int64_t>(tgroup) * a.K_pad + kbase + 32 * q + lane) * a.F,
+                               acc2 + lane_off, h, 32 * q + lane < kvalid);
+          tc_fence_before();
+          mbar_arrive(&S->acc2_empty);
+          ++flush_idx;
+        }
+      }
+    }
+  }
+  // log-likelihood partial of this CTA
+  if (a.mode == MODE_EM) {
+    ll += static_cast<double>(llf);
+    for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, o);
+    if (lane == 0) S->ll_red[warp - 4] = ll;
+    named_bar_sync(1, 256);
+    if (st == 0) {
+      double tot = 0.0;
+      for (int i = 0; i < 8; ++i) tot += S->ll_red[i];
+      a.ll_part[tgroup * C + rank] = tot * kLn2;
+    }
+  }
+}
+
 // ============================================================== fused kernel
-template <int NP, int NCH, int NST>
+// kTopm: the MODE_TOPM instantiation; the others run MODE_EM, MODE_LSE and
+// MODE_GIVEN.  Keeping the top-m code out of the EM instantiations keeps their
+// register allocation for the softmax.
+template <int NP, int NCH, int NST, bool kTopm>
 __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
   using CF = Cfg<NP, NCH, NST>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -579,7 +777,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     S->abort_flag = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S->full_a[i], 128);
-      mbar_init(&S->empty_a[i], 1);
+      for (int g = 0; g < 8; ++g) mbar_init(&S->empty_g[i][g], 1);
       mbar_init(&S->xready[i], 1);
     }
     mbar_init(&S->p_full, 1);
@@ -605,6 +803,13 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       S->iscale[j] = a.iscale[kbase + j];
     }
   }
+  if (tid < 128) {
+    // the all-ones operand that turns the statistics MMA into a row count
+    const uint32_t one2 = 0x3C003C00u;   // pairs of fp16 1.0
+    uint32_t* ones = reinterpret_cast<uint32_t*>(sm + CF::kOffOnes);
+    for (int i = tid; i < 512; i += 128) ones[i] = one2;
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   if (C > 1 && !given) cluster_sync();
@@ -616,14 +821,19 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
   const uint32_t sA = smem_u32(sm + CF::kOffA);
   const uint32_t sP = smem_u32(sm + CF::kOffP);
   const uint32_t sR = smem_u32(sm + CF::kOffR);
+  const uint32_t sOnes = smem_u32(sm + CF::kOffOnes);
   constexpr uint32_t kAbType = 0u;   // fp16 operands (PRECISE: hi and lo pieces)
 
   if (warp < 4) {
     // ================================================= transform warps
-    if (a.x_bf16) transform_warps<CF, NP, NCH, NST, true>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
-    else transform_warps<CF, NP, NCH, NST, false>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
+    if (a.x_bf16) transform_warps<CF, NP, NCH, NST, true, kTopm>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
+    else transform_warps<CF, NP, NCH, NST, false, kTopm>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
+  } else if (warp < 12 && NP == 1 && !kTopm) {
+    // ================================================= softmax warps (FAST EM)
+    softmax_fast<CF>(a, sm, S, abort_flag, tid, warp, lane, rank, C, tgroup, n_tgroups, my_tiles, acc1, acc2,
+                     kbase, kvalid);
   } else if (warp < 12) {
-    // ================================================= softmax warps
+    // ================================================= softmax warps (PRECISE, top-m)
     const int st = tid - 128;            // 0..255
     const int q = warp & 3;              // TMEM lane quarter
     const int h = (warp - 4) >> 2;       // column half
@@ -634,7 +844,6 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     float llf = 0.f;              // fp32 part of ll, moved into ll at every flush
     // the rows of a tile share the log-likelihood work among the CTAs of a cluster
     const bool ll_row = h == 0 && (nl % C) == rank;
-    float s0a = 0.f, s0b = 0.f;   // S0 partials of two components (see column_sums_32)
     int flush_idx = 0;
     int j = 0;
     for (int t = tgroup; j < my_tiles; t += n_tgroups, ++j) {
@@ -674,7 +883,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       m = fmaxf(S->pair_m[0][nl], S->pair_m[1][nl]);
       const float mh = S->pair_m[h][nl];   // maximum over this half (MODE_TOPM keys)
       float ssum = 0.f;
-      if (a.mode == MODE_TOPM) {
+      if (kTopm) {
 #pragma unroll
         for (int e = 0; e < 64; ++e) ssum += m == -CUDART_INF_F ? 0.f : ex2(v[e] - m);
       } else {
@@ -725,7 +934,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
         if (rank == 0 && h == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
         continue;
       }
-      if (a.mode == MODE_TOPM) {
+      if constexpr (kTopm) {
         if (a.topm_groups > 1) {
           if (rank == 0 && h == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
         } else if (ll_row && valid) {
@@ -744,27 +953,35 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
         continue;
       }
       if (a.mode == MODE_EM && ll_row && valid) llf += lse;
-      // r is stored as r * 2^15 in fp16 so that small responsibilities stay
+      // r is stored as r * kRScale in fp16 so that small responsibilities stay
       // out of the fp16 subnormal range; finalize divides the statistics back.
-      const float rscale = 32768.f;
+      const float rscale = kRScale<NP>();
       const float f = (valid && lse > -CUDART_INF_F && m > -CUDART_INF_F) ? ex2(m - lse) * rscale : 0.f;
       // responsibilities of this half-row into the statistics operand
       const int ru = 2 * j + rho;          // use index of the R buffer
       if (ru > 0) mbar_wait(&S->r_empty, (ru - 1) & 1, abort_flag, a.status);
       const int nr = nl - 64 * rho;        // row inside the 64-point half
       uint8_t* rbase = sm + CF::kOffR + h * 8192;
+      if constexpr (NP == 1) {
+        // fp16 pairs of r * kRScale: the R tile
+        uint32_t rw[32];
 #pragma unroll
-      for (int e = 0; e < 64; ++e) v[e] *= f;
+        for (int i = 0; i < 32; ++i) rw[i] = pack_f16x2(v[2 * i] * f, v[2 * i + 1] * f);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float* r8 = v + 8 * c;
-        const uint32_t off = sw128_off(nr, c);
-        if constexpr (NP == 1) {
+        for (int c = 0; c < 8; ++c) {
           uint4 w;
-          w.x = pack_f16x2(r8[0], r8[1]); w.y = pack_f16x2(r8[2], r8[3]);
-          w.z = pack_f16x2(r8[4], r8[5]); w.w = pack_f16x2(r8[6], r8[7]);
-          *reinterpret_cast<uint4*>(rbase + off) = w;
-        } else {
+          w.x = rw[4 * c]; w.y = rw[4 * c + 1]; w.z = rw[4 * c + 2]; w.w = rw[4 * c + 3];
+          *reinterpret_cast<uint4*>(rbase + sw128_off(nr, c)) = w;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&S->r_full);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) v[e] *= f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float* r8 = v + 8 * c;
+          const uint32_t off = sw128_off(nr, c);
           float hi[8], lo[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -779,56 +996,45 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
           w.z = pack_f16x2(lo[4], lo[5]); w.w = pack_f16x2(lo[6], lo[7]);
           *reinterpret_cast<uint4*>(rbase + CF::kRBytes + off) = w;
         }
+        fence_proxy_async_smem();
+        mbar_arrive(&S->r_full);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&S->r_full);
-      // S0: column sums of r over the 32 points (lanes) of this warp; lane l
-      // ends with components 64h + 2l and 64h + 2l + 1, kept across tiles
-      column_sums_32(v, lane);
-      s0a += v[0];
-      s0b += v[1];
       // statistics leave tensor memory at the end of a flush period
       const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
       if (flush && stats) {
-        // S0 partials of the four lane quarters meet in shared memory (the
-        // pair arrays are free here)
-        float* s0red = &S->pair_m[0][0];       // [4][128] over pair_m and pair_s
-        named_bar_sync(1, 256);                 // every read of pair_s of this tile is done
-        s0red[q * 128 + 64 * h + 2 * lane] = s0a;
-        s0red[q * 128 + 64 * h + 2 * lane + 1] = s0b;
-        s0a = 0.f;
-        s0b = 0.f;
         ll += static_cast<double>(llf);
         llf = 0.f;
-        named_bar_sync(1, 256);
         mbar_wait(&S->acc2_full, flush_idx & 1, abort_flag, a.status);
         tc_fence_after();
         // lanes = components 32q + lane; h = 0: S1 and S0, h = 1: S2
         const int kl = 32 * q + lane;
         double* prow = a.part + (static_cast<int64_t>(tgroup) * a.K_pad + kbase + kl) * a.F;
         const int c0 = h == 0 ? 0 : CF::kDp;
+        // Each element of the partials has exactly one writer (this thread),
+        // so fire-and-forget fp64 reductions keep a fixed order of additions
+        // without waiting for the old value.
         for (int c = 0; c < CF::kDp; c += 16) {
           float w[16];
           tmem_ld16(acc2 + lane_off + c0 + c, w);
           tmem_wait_ld();
           if (kl < kvalid) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) prow[c0 + c + e] += static_cast<double>(w[e]);
+            for (int e = 0; e < 16; ++e) red_add_f64(prow + c0 + c + e, static_cast<double>(w[e]));
           }
         }
-        if (h == 0 && kl < kvalid) {
-          const float t0 = s0red[kl] + s0red[128 + kl];
-          const float t1 = s0red[256 + kl] + s0red[384 + kl];
-          prow[2 * CF::kDp] += static_cast<double>(t0) + static_cast<double>(t1);
+        if (h == 0) {
+          float w[16];
+          tmem_ld16(acc2 + lane_off + 2 * CF::kDp, w);
+          tmem_wait_ld();
+          if (kl < kvalid) red_add_f64(prow + 2 * CF::kDp, static_cast<double>(w[0]));
         }
         tc_fence_before();
         mbar_arrive(&S->acc2_empty);
         ++flush_idx;
-        named_bar_sync(1, 256);    // s0red is read before the pair arrays are reused
       }
     }
     // log-likelihood partial of this cluster (rank 0 only)
-    if (a.mode == MODE_EM || (a.mode == MODE_TOPM && a.topm_groups == 1)) {
+    if (a.mode == MODE_EM || (kTopm && a.topm_groups == 1)) {
       ll += static_cast<double>(llf);
       for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, o);
       if (lane == 0) S->ll_red[warp - 4] = ll;
@@ -852,9 +1058,10 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
 
       const uint32_t id1 = idesc_f16(kAbType, 0, 0, 128, n1);
       const uint32_t id2 = idesc_f16(kAbType, 1, 1, 128, 2 * CF::kDp);
+      const uint32_t id0 = idesc_f16(kAbType, 1, 1, 128, 16);
       int flush_idx = 0;
       bool fresh = true;   // next statistics MMA starts a new accumulation
-      const int nst = a.mode == MODE_TOPM ? 1 : NST;   // MODE_TOPM: stage 1 holds the lists
+      const int nst = kTopm ? 1 : NST;   // MODE_TOPM: stage 1 holds the lists
 
       auto issue_g1 = [&](int jj) {
         const int s = jj % nst;
@@ -882,7 +1089,8 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       if (my_tiles > 0) {
         wait_a(0);
         issue_g1(0);
-        if (!stats) mma_commit(&S->empty_a[0]);
+        if (!stats)
+          for (int g = 0; g < 8; ++g) mma_commit(&S->empty_g[0][g]);
       }
       for (int j = 0; j < my_tiles; ++j) {
         if (*abort_flag) break;
@@ -894,7 +1102,8 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
             mbar_wait(&S->acc1_empty, j & 1, abort_flag, a.status);
             tc_fence_after();
             issue_g1(j + 1);
-            if (!stats) mma_commit(&S->empty_a[(j + 1) % nst]);
+            if (!stats)
+              for (int g = 0; g < 8; ++g) mma_commit(&S->empty_g[(j + 1) % nst][g]);
           }
         }
         if (stats) {
@@ -906,21 +1115,32 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
           for (int rho = 0; rho < 2; ++rho) {
             mbar_wait(&S->r_full, rho, abort_flag, a.status);
             tc_fence_after();
+            for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-            for (int pr = 0; pr < (NP == 1 ? 1 : 3); ++pr) {
-              const int prr = pr == 2 ? 1 : 0;   // responsibility piece
-              const int pf = pr == 1 ? 1 : 0;    // data piece
-              for (int kk = 0; kk < 4; ++kk) {
+              for (int pr = 0; pr < (NP == 1 ? 1 : 3); ++pr) {
+                const int prr = pr == 2 ? 1 : 0;   // responsibility piece
+                const int pf = pr == 1 ? 1 : 0;    // data piece
                 const uint64_t ad = sdesc_sw128(sR + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
                 const uint64_t bd = sdesc_sw128(stage + pf * CF::kPieceBytes + rho * 8192 + 2048 * kk,
                                                 kChunkBytes, 1024);
                 mma_f16_ss(acc2, ad, bd, id2, fresh ? 0u : 1u);
                 fresh = false;
               }
+              // rows 16 (4 rho + kk) .. +15 of the stage are no longer needed
+              mma_commit(&S->empty_g[s][4 * rho + kk]);
             }
+            // S0: responsibilities against an all-ones operand (the same fp16
+            // values as S1 and S2, summed in fp32 by the tensor core)
+            bool fresh0 = (rho == 0) && (j % a.flush_tiles == 0);
+            for (int prr = 0; prr < NP; ++prr)
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sdesc_sw128(sR + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
+                const uint64_t bd = sdesc_sw128(sOnes, kChunkBytes, 1024);
+                mma_f16_ss(acc2 + 2 * CF::kDp, ad, bd, id0, fresh0 ? 0u : 1u);
+                fresh0 = false;
+              }
             mma_commit(&S->r_empty);
           }
-          mma_commit(&S->empty_a[s]);
           const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
           if (flush) {
             mma_commit(&S->acc2_full);
@@ -1122,9 +1342,12 @@ const void* kernel_handle(KernelId id) {
     case K_META: return reinterpret_cast<const void*>(&meta_kernel);
     case K_PARAMS_FAST: return reinterpret_cast<const void*>(&params_kernel<true>);
     case K_PARAMS_PRECISE: return reinterpret_cast<const void*>(&params_kernel<false>);
-    case K_FUSED_1_1_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 1, 2>);
-    case K_FUSED_1_2_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 2, 2>);
-    case K_FUSED_2_1_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 1, 1>);
+    case K_FUSED_1_1_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 1, 2, false>);
+    case K_FUSED_1_2_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 2, 2, false>);
+    case K_FUSED_2_1_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 1, 1, false>);
+    case K_TOPM_1_1_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 1, 2, true>);
+    case K_TOPM_1_2_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 2, 2, true>);
+    case K_TOPM_2_1_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 1, 1, true>);
     case K_LSE_COMBINE: return reinterpret_cast<const void*>(&lse_combine_kernel);
     case K_FINALIZE: return reinterpret_cast<const void*>(&finalize_kernel);
     case K_TOPM_COMBINE: return reinterpret_cast<const void*>(&topm_combine_kernel);

@@ -9,6 +9,12 @@ namespace gmm {
 
 constexpr int kMaxD = 128;
 
+// Scale of the fp16 responsibility operand: r is stored as r * kRScale, so
+// that responsibilities down to 2^-24 / kRScale stay out of the fp16
+// subnormal range (FAST, one piece: 2^10; PRECISE, hi + lo pieces: 2^15).
+template <int NP>
+__host__ __device__ constexpr float kRScale() { return NP == 1 ? 1024.f : 32768.f; }
+
 // Device status bits (or-ed into a word in global memory).
 enum : uint32_t {
   ST_TIMEOUT = 1u,
@@ -27,7 +33,7 @@ struct Meta {
 enum KernelId : int {
   K_ABSMAX, K_ABSMAX_VEC, K_META, K_PARAMS_FAST, K_PARAMS_PRECISE,
   K_FUSED_1_1_2, K_FUSED_1_2_2, K_FUSED_2_1_1, K_LSE_COMBINE, K_FINALIZE,
-  K_TOPM_COMBINE, K_LL_TOTAL,
+  K_TOPM_COMBINE, K_LL_TOTAL, K_TOPM_1_1_2, K_TOPM_1_2_2, K_TOPM_2_1_1,
 };
 
 // Host-side handle of a kernel, for cudaLaunchKernelEx (argument order and
@@ -79,7 +85,7 @@ struct Small {
   float lse_row[kBN];     // MODE_TOPM: normaliser of each row of the tile (log2 units)
   double ll_red[8];
   uint64_t full_a[2];
-  uint64_t empty_a[2];
+  uint64_t empty_g[2][8];  // per stage: 16-row group g no longer read by the MMAs
   uint64_t p_full;
   uint64_t acc1_full;
   uint64_t acc1_empty;
@@ -97,7 +103,7 @@ struct Small {
 
 // Shared-memory plan of the fused kernel for NP operand pieces (1: fp16,
 // 2: fp16 hi/lo), NCH 64-feature atom columns per data part, NST data stages:
-//   [data stages | parameter image | Small | R tile]
+//   [data stages | parameter image | Small | R tile | ones]
 // MODE_TOPM runs with one data stage; the second stage (or, with a single
 // stage, the R tile area) holds the per-row candidate lists.
 template <int NP, int NCH, int NST>
@@ -109,9 +115,10 @@ struct Cfg {
   static constexpr int kOffSmall = kOffP + NP * kPieceBytes;
   static constexpr int kOffR = (kOffSmall + static_cast<int>(sizeof(Small)) + 1023) / 1024 * 1024;
   static constexpr int kRBytes = 64 * kSlice * 2;                     // 64 points x 128 comps x 16 bit
-  static constexpr int kEnd = kOffR + NP * kRBytes;
+  static constexpr int kOffOnes = kOffR + NP * kRBytes;             // 16 x 64 fp16 ones
+  static constexpr int kEnd = kOffOnes + 2048;
   static constexpr int kDp = NCH * kAtomElems;
-  static constexpr int kF2 = 2 * kDp;                                 // statistics columns in TMEM
+  static constexpr int kF2 = 2 * kDp + 16;                            // statistics columns in TMEM
   static constexpr uint32_t kAcc1Col = 0;
   static constexpr uint32_t kAcc2Col = 128;
   static constexpr int kThreads = 13 * 32;
