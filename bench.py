@@ -175,9 +175,9 @@ def run_reference(args, w, ws, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, precision):
+def config_of(w, precision, plan="auto"):
     return {"workload": w.name, "N": w.N, "D": w.D, "K": w.K, "cov": w.cov, "x_dtype": w.x_dtype,
-            "precision": precision, "parallelism": "replicas",
+            "precision": precision, "plan": plan, "parallelism": "replicas",
             "l2": "inputs larger than L2 (no flush)" if w.N * w.D * (2 if w.x_dtype == "bf16" else 4) > 126e6
             else "L2 flushed between steps"}
 
@@ -193,8 +193,8 @@ def run_ours(args, w, ws, rank, local):
     flush = None
     if x_bytes <= 126e6:
         flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
-    opts = G.gmm_default_opts(precision=args.precision)
-    G.gmm_reserve(w.N, w.D, w.K, w.cov, w.x_dtype, precision=args.precision)
+    opts = G.gmm_default_opts(precision=args.precision, plan=args.plan)
+    G.gmm_reserve(w.N, w.D, w.K, w.cov, w.x_dtype, precision=args.precision, plan=args.plan)
 
     def step():
         if flush is not None:
@@ -287,7 +287,7 @@ def run_ours(args, w, ws, rank, local):
         "metric": METRIC, "value": ws * 1e3 / ms_max, "unit": "EM iter/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-        "data": "synthetic", "config": config_of(w, args.precision),
+        "data": "synthetic", "config": config_of(w, args.precision, args.plan),
         "nkd_per_s": ws * w.N * w.K * w.D * 1e3 / ms_max,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
@@ -324,6 +324,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="embed_10m", choices=sorted(W.WORKLOADS))
     ap.add_argument("--precision", default="auto", choices=["auto", "fast", "precise"])
+    ap.add_argument("--plan", default="auto", choices=["auto", "cluster", "split"])
     ap.add_argument("--rows", type=int, default=0,
                     help="run on the first ROWS rows of the workload (profiling a smaller case)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -23,6 +23,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "gmm.h")
 SPHERICAL, DIAG = 0, 1
 F32, BF16 = 0, 1
 PREC = {"auto": 0, "fast": 1, "precise": 2}
+PLAN = {"auto": 0, "cluster": 1, "split": 2}
 COV = {"spherical": SPHERICAL, "diag": DIAG}
 STATUS = {0: "GMM_OK", -1: "GMM_ERR_INVALID_ARG", -2: "GMM_ERR_UNSUPPORTED",
           -3: "GMM_ERR_NONFINITE", -4: "GMM_ERR_CUDA", -5: "GMM_ERR_TIMEOUT", -6: "GMM_ERR_RANGE"}
@@ -37,7 +38,7 @@ class GmmError(RuntimeError):
 class gmm_opts(ctypes.Structure):
     _fields_ = [("precision", ctypes.c_int32), ("reg_covar", ctypes.c_float),
                 ("var_floor", ctypes.c_float), ("x_absmax", ctypes.c_float),
-                ("loglik_on_host", ctypes.c_int32)]
+                ("loglik_on_host", ctypes.c_int32), ("plan", ctypes.c_int32)]
 
 
 _lib = None
@@ -103,6 +104,8 @@ def gmm_default_opts(**kw) -> gmm_opts:
     for k, v in kw.items():
         if k == "precision" and isinstance(v, str):
             v = PREC[v]
+        if k == "plan" and isinstance(v, str):
+            v = PLAN[v]
         setattr(o, k, v)
     return o
 

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -50,7 +51,8 @@ struct Plan {
   int K_pad, n_slices;
   int n_tiles;
   bool two_pass;
-  int C;              // cluster size of the single pass / of pass 1
+  int C;              // cluster size of the single pass
+  int C1;             // cluster size of pass 1 (two-pass): 8, or 1 in the SPLIT plan
   int n_kgroups;      // pass 1 K groups (two-pass)
   int tg;             // tile groups of the statistics pass
   int tg1;            // tile groups of pass 1 (two-pass)
@@ -143,6 +145,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   if (dtype != GMM_F32 && dtype != GMM_BF16) return fail(GMM_ERR_INVALID_ARG, "x_dtype must be 0 or 1");
   if (o.precision < GMM_PREC_AUTO || o.precision > GMM_PREC_PRECISE)
     return fail(GMM_ERR_INVALID_ARG, "unknown precision");
+  if (o.plan < GMM_PLAN_AUTO || o.plan > GMM_PLAN_SPLIT) return fail(GMM_ERR_INVALID_ARG, "unknown plan");
   if (!(o.reg_covar >= 0.f) || !(o.var_floor >= 0.f) || !std::isfinite(o.reg_covar) || !std::isfinite(o.var_floor))
     return fail(GMM_ERR_INVALID_ARG, "reg_covar and var_floor must be finite and >= 0");
   if (!(o.x_absmax >= 0.f) || !std::isfinite(o.x_absmax)) return fail(GMM_ERR_INVALID_ARG, "x_absmax must be finite and >= 0");
@@ -158,8 +161,10 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.nst = p.fast ? 2 : 1;
   if (!p.fast && p.nch != 1) return fail(GMM_ERR_UNSUPPORTED, "PRECISE arithmetic supports D <= 64");
   p.n_slices = (K + kSlice - 1) / kSlice;
-  p.two_pass = p.n_slices > 8;
-  if (p.two_pass) p.n_slices = (p.n_slices + 7) / 8 * 8;   // whole 8-slice groups for pass 1
+  const bool split = o.plan == GMM_PLAN_SPLIT;
+  p.two_pass = split || p.n_slices > 8;
+  p.C1 = split ? 1 : 8;
+  if (p.two_pass && !split) p.n_slices = (p.n_slices + 7) / 8 * 8;   // whole 8-slice groups for pass 1
   p.K_pad = p.n_slices * kSlice;
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
   p.smem = fused_smem(p.np, p.nch, p.nst);
@@ -174,9 +179,9 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
     p.tg = std::max(1, std::min(p.n_tiles, mc));
     p.tg1 = 0;
   } else {
-    p.C = 8;
-    p.n_kgroups = (p.n_slices + 7) / 8;
-    int mc = need_device ? max_clusters(fn, p.smem, 8) : std::max(1, sms / 8);
+    p.C = p.C1;
+    p.n_kgroups = p.n_slices / p.C1;
+    int mc = p.C1 == 1 ? sms : (need_device ? max_clusters(fn, p.smem, p.C1) : std::max(1, sms / p.C1));
     p.tg1 = std::max(1, std::min(p.n_tiles, mc / p.n_kgroups));
     p.tg = std::max(1, std::min(p.n_tiles, sms / p.n_slices));
   }
@@ -234,8 +239,13 @@ int get_workspace(size_t need, uint8_t** out) {
   return GMM_OK;
 }
 
-int status_to_code(uint32_t st) {
-  if (st & ST_TIMEOUT) return fail(GMM_ERR_TIMEOUT, "a device-side wait exceeded its bound");
+int status_to_code(uint32_t st, uint32_t where = 0) {
+  if (st & ST_TIMEOUT) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "a device-side wait exceeded its bound (first: thread %u, barrier at shared offset 0x%x)",
+             (where >> 20) & 0x7FFu, where & 0xFFFFFu);
+    return fail(GMM_ERR_TIMEOUT, where ? std::string(buf) : std::string("a device-side wait exceeded its bound"));
+  }
   if (st & ST_NONFINITE) return fail(GMM_ERR_NONFINITE, "a parameter is not finite or a variance is not positive");
   if (st & ST_RANGE) return fail(GMM_ERR_RANGE, "data magnitude outside the FAST operand range");
   return GMM_OK;
@@ -369,6 +379,7 @@ void gmm_default_opts(gmm_opts* o) {
   o->var_floor = 0.f;
   o->x_absmax = 0.f;
   o->loglik_on_host = 0;
+  o->plan = GMM_PLAN_AUTO;
 }
 
 const char* gmm_last_error(void) { return g_error.c_str(); }
@@ -434,8 +445,8 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
     // pass 1: per-point normaliser over each group of 1024 components
     FusedArgs a1 = a;
     a1.mode = MODE_LSE;
-    a1.C = 8;
-    if ((r = launch_main(fn, dim3(8 * p.tg1, p.n_kgroups), dim3(416), p.smem, s, 8, a1))) return r;
+    a1.C = p.C1;
+    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), p.smem, s, p.C1, a1))) return r;
     float* lse = reinterpret_cast<float*>(ws + p.off_lse);
     if ((r = launch(kernel_handle(K_LSE_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
                     static_cast<const float*>(a.lse_part), p.n_kgroups, p.N, lse,
@@ -462,11 +473,11 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
   if (o.loglik_on_host) {
     CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
     CUDA_TRY(cudaStreamSynchronize(s));
-    uint32_t st = 0;
-    CUDA_TRY(cudaMemcpy(&st, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost));
-    if (st) {
-      CUDA_TRY(cudaMemset(ws, 0, sizeof(uint32_t)));
-      return status_to_code(st);
+    uint32_t st[2] = {0, 0};
+    CUDA_TRY(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
+    if (st[0]) {
+      CUDA_TRY(cudaMemset(ws, 0, sizeof(st)));
+      return status_to_code(st[0], st[1]);
     }
   }
   return GMM_OK;
@@ -520,11 +531,11 @@ int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov
                               static_cast<const double*>(a.ll_part), p.tg * p.C, ll_dev)))
       return r;
   } else {
-    a.C = 8;
+    a.C = p.C1;
     a.topm_groups = p.n_kgroups;
     a.topm_val = reinterpret_cast<float*>(ws + off_gval);
     a.topm_idx = reinterpret_cast<int32_t*>(ws + off_gidx);
-    if ((r = launch_main(fn, dim3(8 * p.tg1, p.n_kgroups), dim3(416), smem, s, 8, a))) return r;
+    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), smem, s, p.C1, a))) return r;
     if ((r = launch(kernel_handle(K_TOPM_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
                     static_cast<const float*>(a.lse_part), static_cast<const float*>(a.topm_val),
                     static_cast<const int32_t*>(a.topm_idx), p.n_kgroups, p.N, m, resp_out, idx_out,
@@ -537,11 +548,11 @@ int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov
   if (o.loglik_on_host) {
     CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
     CUDA_TRY(cudaStreamSynchronize(s));
-    uint32_t st = 0;
-    CUDA_TRY(cudaMemcpy(&st, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost));
-    if (st) {
-      CUDA_TRY(cudaMemset(ws, 0, sizeof(uint32_t)));
-      return status_to_code(st);
+    uint32_t st[2] = {0, 0};
+    CUDA_TRY(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
+    if (st[0]) {
+      CUDA_TRY(cudaMemset(ws, 0, sizeof(st)));
+      return status_to_code(st[0], st[1]);
     }
   }
   return GMM_OK;
@@ -558,10 +569,10 @@ int gmm_stream_status(void* stream) {
     if (it == g_ws.end() || !it->second.buf) return GMM_OK;
     buf = it->second.buf;
   }
-  uint32_t st = 0;
-  CUDA_TRY(cudaMemcpy(&st, buf, sizeof(uint32_t), cudaMemcpyDeviceToHost));
-  if (st) CUDA_TRY(cudaMemset(buf, 0, sizeof(uint32_t)));
-  return status_to_code(st);
+  uint32_t st[2] = {0, 0};
+  CUDA_TRY(cudaMemcpy(st, buf, sizeof(st), cudaMemcpyDeviceToHost));
+  if (st[0]) CUDA_TRY(cudaMemset(buf, 0, sizeof(st)));
+  return status_to_code(st[0], st[1]);
 }
 
 void gmm_profile_begin(void) {
@@ -665,6 +676,7 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
       (r = check_ptr(new_means, "new_means")) || (r = check_ptr(new_vars, "new_vars")))
     return r;
   if (!total_loglik) return fail(GMM_ERR_INVALID_ARG, "total_loglik is NULL");
+  o.plan = GMM_PLAN_CLUSTER;   // the single pass: no N-sized buffer
   Plan p;
   if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
   if (p.two_pass)
@@ -697,9 +709,9 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const void* fn = fused_fn(p.np, p.nch, p.nst);
   if ((r = set_smem_attr(fn, p.smem))) return r;
-  // the array keeps the previous call's contents: clear the status word and
+  // the array keeps the previous call's contents: clear the status words and
   // the statistics accumulators, which must start at zero
-  CUDA_TRY(cudaMemsetAsync(ws, 0, sizeof(uint32_t), s));
+  CUDA_TRY(cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s));
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
   CUDA_TRY(cudaMemsetAsync(ws + p.off_part, 0, row_bytes * p.tg, s));
   FusedArgs a = base_args(p, X, ws);
@@ -720,9 +732,9 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
   if (o.loglik_on_host) {
     CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
     CUDA_TRY(cudaStreamSynchronize(s));
-    uint32_t st = 0;
-    CUDA_TRY(cudaMemcpy(&st, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost));
-    if (st) return status_to_code(st);
+    uint32_t st[2] = {0, 0};
+    CUDA_TRY(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
+    if (st[0]) return status_to_code(st[0], st[1]);
   }
   return GMM_OK;
 }

@@ -564,7 +564,8 @@ __device__ __forceinline__ void flush_stats(double* prow, uint32_t taddr, int h,
 //         the statistics MMA, and the periodic flush of the statistics.
 // Two receive slots are safe: a CTA pushes tile t only after its B(t-1),
 // which needs every CTA's push of t-1, which each makes only after its own
-// B(t-2) has read the slot that tile t reuses.
+// B(t-2) has read the slot that tile t reuses (and after the copies of
+// tile t-2 out of its own chunk had landed).
 // The two warps that share a lane quarter (one per column half) meet at a
 // named barrier of their own.
 template <typename CF>
@@ -647,13 +648,23 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
       const float tot = S->pair_s[0][nl] + S->pair_s[1][nl];
       lse_loc = tot > 0.f ? m + lg2(tot) - kLog2R : -CUDART_INF_F;
     }
-    // push this CTA's row normalisers of tile j to every CTA of the cluster
+    // push this CTA's row normalisers of tile j to every other CTA of the
+    // cluster: each warp of column half 0 writes its 32 rows into its own
+    // chunk of the slot and one lane bulk-copies the 128-byte chunk to the
+    // same place in every peer (one transaction per chunk and peer)
     if (exch && h == 0) {
-      const uint32_t dst = smem_u32(&S->xrecv[j & 1][rank][nl]);
-      const uint32_t bar = smem_u32(&S->xready[j & 1]);
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        if (r < C) st_async_f32(mapa(dst, r), lse_loc, mapa(bar, r));
+      if (lane == 0) bulk_wait_read_all();     // the previous copies have read the chunk
+      __syncwarp();
+      S->xrecv[j & 1][rank][nl] = lse_loc;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t src = smem_u32(&S->xrecv[j & 1][rank][32 * q]);
+        const uint32_t bar = smem_u32(&S->xready[j & 1]);
+        for (int r = 0; r < C; ++r)
+          if (r != rank) bulk_s2c(mapa(src, r), src, 128u, mapa(bar, r));
+        bulk_commit_group();
+      }
     }
     // ---------------------------------------------------------------- B(j): normalise, R tile
     const int64_t pn = static_cast<int64_t>(tgroup + j * n_tgroups) * kBN + nl;
@@ -667,11 +678,12 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
         lse = valid ? __ldg(a.lse_in + pn) : -CUDART_INF_F;
       } else if (C > 1) {
         const int slot = jj & 1;
-        if (st == 0) mbar_arrive_expect_tx(&S->xready[slot], static_cast<uint32_t>(C * kBN * 4));
+        if (st == 0) mbar_arrive_expect_tx(&S->xready[slot], static_cast<uint32_t>((C - 1) * kBN * 4));
         mbar_wait(&S->xready[slot], (jj >> 1) & 1, abort_flag, a.status);
         float vals[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) vals[r] = r < C ? S->xrecv[slot][r][nl] : -CUDART_INF_F;
+        for (int r = 0; r < 8; ++r)
+          vals[r] = r == rank ? lse_loc : (r < C ? S->xrecv[slot][r][nl] : -CUDART_INF_F);
         float mx = vals[0];
 #pragma unroll
         for (int r = 1; r < 8; ++r) mx = fmaxf(mx, vals[r]);
@@ -694,8 +706,14 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
           x = __hmul2(x, f2);
           pk[i] = *reinterpret_cast<uint32_t*>(&x);
         }
-        const int ru = 2 * jj + rho;      // use index of the R buffer
-        if (ru > 0) mbar_wait(&S->r_empty, (ru - 1) & 1, abort_flag, a.status);
+        // the R buffer is free once the statistics MMA has read the previous
+        // half written into it: half 1 of tile jj-1 for rows 0-63, half 0 of
+        // tile jj for rows 64-127 (one barrier per half, one phase per tile)
+        if (rho == 0) {
+          if (jj > 0) mbar_wait(&S->r_done[1], (jj - 1) & 1, abort_flag, a.status);
+        } else {
+          mbar_wait(&S->r_done[0], jj & 1, abort_flag, a.status);
+        }
         uint8_t* rbase = sm + CF::kOffR + h * 8192;
         const int nr = nl - 64 * rho;
 #pragma unroll
@@ -705,7 +723,7 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
           *reinterpret_cast<uint4*>(rbase + sw128_off(nr, c)) = w;
         }
         fence_proxy_async_smem();
-        mbar_arrive(&S->r_full);
+        mbar_arrive(&S->r_full[rho]);
         // statistics leave tensor memory at the end of a flush period
         if (((jj + 1) % a.flush_tiles == 0) || (jj + 1 == my_tiles)) {
           ll += static_cast<double>(llf);
@@ -783,8 +801,10 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     mbar_init(&S->p_full, 1);
     mbar_init(&S->acc1_full, 1);
     mbar_init(&S->acc1_empty, 256);
-    mbar_init(&S->r_full, 128);
-    mbar_init(&S->r_empty, 1);
+    mbar_init(&S->r_full[0], 128);
+    mbar_init(&S->r_full[1], 128);
+    mbar_init(&S->r_done[0], 1);
+    mbar_init(&S->r_done[1], 1);
     mbar_init(&S->acc2_full, 1);
     mbar_init(&S->acc2_empty, 256);
     mbar_init(&S->drain, 1);
@@ -958,8 +978,13 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       const float rscale = kRScale<NP>();
       const float f = (valid && lse > -CUDART_INF_F && m > -CUDART_INF_F) ? ex2(m - lse) * rscale : 0.f;
       // responsibilities of this half-row into the statistics operand
-      const int ru = 2 * j + rho;          // use index of the R buffer
-      if (ru > 0) mbar_wait(&S->r_empty, (ru - 1) & 1, abort_flag, a.status);
+      // the R buffer is free once the statistics MMA has read the previous half
+      // written into it (one barrier per half, one phase per tile)
+      if (rho == 0) {
+        if (j > 0) mbar_wait(&S->r_done[1], (j - 1) & 1, abort_flag, a.status);
+      } else {
+        mbar_wait(&S->r_done[0], j & 1, abort_flag, a.status);
+      }
       const int nr = nl - 64 * rho;        // row inside the 64-point half
       uint8_t* rbase = sm + CF::kOffR + h * 8192;
       if constexpr (NP == 1) {
@@ -974,7 +999,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
           *reinterpret_cast<uint4*>(rbase + sw128_off(nr, c)) = w;
         }
         fence_proxy_async_smem();
-        mbar_arrive(&S->r_full);
+        mbar_arrive(&S->r_full[rho]);
       } else {
 #pragma unroll
         for (int e = 0; e < 64; ++e) v[e] *= f;
@@ -997,7 +1022,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
           *reinterpret_cast<uint4*>(rbase + CF::kRBytes + off) = w;
         }
         fence_proxy_async_smem();
-        mbar_arrive(&S->r_full);
+        mbar_arrive(&S->r_full[rho]);
       }
       // statistics leave tensor memory at the end of a flush period
       const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
@@ -1113,7 +1138,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
             tc_fence_after();
           }
           for (int rho = 0; rho < 2; ++rho) {
-            mbar_wait(&S->r_full, rho, abort_flag, a.status);
+            mbar_wait(&S->r_full[rho], j & 1, abort_flag, a.status);
             tc_fence_after();
             for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
@@ -1139,7 +1164,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
                 mma_f16_ss(acc2 + 2 * CF::kDp, ad, bd, id0, fresh0 ? 0u : 1u);
                 fresh0 = false;
               }
-            mma_commit(&S->r_empty);
+            mma_commit(&S->r_done[rho]);
           }
           const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
           if (flush) {

@@ -89,8 +89,8 @@ struct Small {
   uint64_t p_full;
   uint64_t acc1_full;
   uint64_t acc1_empty;
-  uint64_t r_full;
-  uint64_t r_empty;
+  uint64_t r_full[2];     // half rho of the R tile written (128 threads), one phase per tile
+  uint64_t r_done[2];     // half rho of the R tile read by the statistics MMA
   uint64_t acc2_full;
   uint64_t acc2_empty;
   uint64_t xready[2];     // slot filled: every CTA of the cluster has pushed its row normalisers

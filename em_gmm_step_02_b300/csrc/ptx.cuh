@@ -105,6 +105,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+// Records, for the first wait of a launch to give up, which barrier (its
+// shared-memory offset) and which thread, in status[1] (status[0] carries the
+// flags).
+__device__ __forceinline__ void note_timeout(const uint64_t* bar, uint32_t* status) {
+  const uint32_t info = 0x80000000u | ((threadIdx.x & 0x7FFu) << 20) | (smem_u32(bar) & 0xFFFFFu);
+  atomicCAS(status + 1, 0u, info);
+}
+
 // Polls allowed per wait before it is declared failed.  try_wait itself
 // suspends for a hardware-chosen interval, so this bounds the wait at a few
 // seconds at most.
@@ -120,6 +128,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
   *abort = 1u;
   atomicOr(status, ST_TIMEOUT);
+  note_timeout(bar, status);
   return false;
 }
 
@@ -140,6 +149,25 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void st_async_f32(uint32_t caddr, float v, uint32_t cbar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                :: "r"(caddr), "r"(__float_as_uint(v)), "r"(cbar) : "memory");
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory (src) to shared memory
+// of a CTA of the cluster (cluster address dst), completing `bytes`
+// transaction bytes on the mbarrier at cluster address cbar (in the
+// destination CTA).  Addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2c(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t cbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "r"(src), "r"(bytes), "r"(cbar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until the bulk copies committed by this thread have read their source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- proxies

@@ -76,6 +76,21 @@ typedef enum {
     GMM_ERR_RANGE = -6          /* data too large for the FAST operand range */
 } gmm_status_t;
 
+/* Launch plan of one EM step (or top-m pass).
+ *  CLUSTER: one pass over X; the CTAs that hold the 128-component slices of
+ *           one point tile form a thread-block cluster and exchange their
+ *           per-row normalisers through distributed shared memory
+ *           (K <= 1024; above that, the normaliser pass below runs with
+ *           clusters of 8 slices and per-cluster partial normalisers).
+ *  SPLIT:   two passes; the first computes every slice's per-row normaliser
+ *           independently (no clusters) into an N x slices buffer, a small
+ *           kernel combines them, and the second pass recomputes the logits
+ *           and accumulates the statistics with the normaliser read from
+ *           memory.  1.5 times the tensor-core work, no cross-CTA waits,
+ *           N * ceil(K / 128) + N extra floats of workspace.
+ *  AUTO:    the faster of the two for the shape (see gmm_em_step). */
+typedef enum { GMM_PLAN_AUTO = 0, GMM_PLAN_CLUSTER = 1, GMM_PLAN_SPLIT = 2 } gmm_plan_t;
+
 typedef struct {
     int32_t precision;       /* gmm_precision_t, default AUTO */
     float reg_covar;         /* added to every new variance, default 1e-6 */
@@ -83,6 +98,7 @@ typedef struct {
     float x_absmax;          /* > 0: caller's bound on max |X| (skips a scan of X) */
     int32_t loglik_on_host;  /* 1: total_loglik is a host pointer; the call waits
                                 for the stream and reports device-side errors */
+    int32_t plan;            /* gmm_plan_t, default AUTO */
 } gmm_opts;
 
 /* Fill *opts with the defaults listed above. */

@@ -90,6 +90,64 @@ def test_one_step_small(N, D, K, cov, xd, prec):
     print(one_step_case(w, precision=prec))
 
 
+SPLIT_CASES = [
+    (4096, 8, 16, "diag", "f32", "auto"),
+    (3777, 17, 129, "spherical", "f32", "auto"),
+    (20000, 128, 1024, "diag", "bf16", "auto"),
+    (12000, 32, 1100, "diag", "bf16", "auto"),
+    (3001, 96, 200, "diag", "bf16", "auto"),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("N,D,K,cov,xd,prec", SPLIT_CASES)
+def test_one_step_small_split_plan(N, D, K, cov, xd, prec):
+    """The two-pass plan (normalisers through memory) against the oracle."""
+    w = W.generic(N, D, K, cov, xd, seed=N + D + K)
+    X = W.make_data(w)
+    init = W.make_init(w, X)
+    ref = oracle.em_step(X.float().numpy(), *init, w.cov)
+    got = run_gpu(X, *init, w.cov, prec, plan="split")
+    path = "fast" if xd == "bf16" else "precise"
+    print(compare(got, ref, X.shape[0], w.cov, path))
+
+
+def _moments_ok(X, lw2, mu2, var2, reg=1e-6):
+    N = X.shape[0]
+    pi = torch.exp(lw2.double())
+    assert abs(pi.sum().item() - 1.0) < 1e-5
+    Nk = pi * N
+    s1 = (Nk[:, None] * mu2.double()).sum(0)
+    xs = X.double().sum(0)
+    assert ((s1 - xs).abs() / X.double().abs().sum(0)).max().item() < 2e-3
+    s2 = (Nk[:, None] * (var2.double() - reg + mu2.double() ** 2)).sum(0)
+    x2 = (X.double() ** 2).sum(0)
+    assert ((s2 - x2).abs() / x2).max().item() < 2e-2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("K,plan", [(100, "cluster"), (100, "split"), (1000, "split")])
+def test_long_run_moments_and_plans_agree(K, plan):
+    """Two million points: enough tiles per CTA for every hand-off of the
+    pipeline to wrap many times (a single 128-component slice runs without
+    the cluster exchange, the fastest schedule).  Moments are conserved and
+    the result agrees with the other plan."""
+    w = W.generic(2_000_000, 128, K, "diag", "bf16", seed=3)
+    X = W.make_data(w, device="cuda")
+    init = W.make_init(w, X)
+    p = params_to_device(*init)
+    a = G.gmm_em_step(X, *p, w.cov, plan=plan)
+    torch.cuda.synchronize()
+    assert G.gmm_stream_status() == 0, G.gmm_last_error()
+    _moments_ok(X, *a[:3])
+    other = "split" if plan == "cluster" else "cluster"
+    b = G.gmm_em_step(X, *p, w.cov, plan=other)
+    torch.cuda.synchronize()
+    assert G.gmm_stream_status() == 0, G.gmm_last_error()
+    assert rel_l2_rows(a[1].cpu().numpy(), b[1].cpu().numpy()).max() < 2e-2
+    assert abs(a[3].item() - b[3].item()) / X.shape[0] < 1e-2
+
+
 @pytest.mark.gpu
 def test_tiny_workload_20_iterations():
     w = W.WORKLOADS["tiny_diag"]
@@ -189,25 +247,17 @@ def test_nonpositive_variance_is_reported():
 
 @pytest.mark.gpu
 def test_conservation_of_moments_full_size_embed():
-    """Full 10M x 128 x 1024 workload in the benchmark's launch configuration:
-    properties that hold at any size (weights sum to 1; sum_k N_k mu_k equals
-    the data sum; sum_k N_k (s2_k + mu_k^2) equals the sum of squares)."""
+    """Full 10M x 128 x 1024 workload in the benchmark's launch configurations
+    (both plans): properties that hold at any size (weights sum to 1;
+    sum_k N_k mu_k equals the data sum; sum_k N_k (s2_k + mu_k^2) equals the
+    sum of squares)."""
     w = W.WORKLOADS["embed_10m"]
     X = W.make_data(w, device="cuda")
     lw, mu, var = W.make_init(w, X)
     p = params_to_device(lw, mu, var)
-    lw2, mu2, var2, ll = G.gmm_em_step(X, *p, w.cov)
-    torch.cuda.synchronize()
-    assert G.gmm_stream_status() == 0
-    N = X.shape[0]
-    pi = torch.exp(lw2.double())
-    assert abs(pi.sum().item() - 1.0) < 1e-5
-    Nk = pi * N
-    s1 = (Nk[:, None] * mu2.double()).sum(0)
-    xs = X.double().sum(0)
-    scale = X.double().abs().sum(0)
-    assert ((s1 - xs).abs() / scale).max().item() < 2e-3
-    s2 = (Nk[:, None] * (var2.double() - 1e-6 + mu2.double() ** 2)).sum(0)
-    x2 = (X.double() ** 2).sum(0)
-    assert ((s2 - x2).abs() / x2).max().item() < 2e-2
-    assert np.isfinite(ll.item())
+    for plan in ("cluster", "split"):
+        lw2, mu2, var2, ll = G.gmm_em_step(X, *p, w.cov, plan=plan)
+        torch.cuda.synchronize()
+        assert G.gmm_stream_status() == 0, G.gmm_last_error()
+        _moments_ok(X, lw2, mu2, var2)
+        assert np.isfinite(ll.item())
