@@ -34,6 +34,9 @@ import workloads as W  # noqa: E402
 
 METRIC = "EM iter/s and N·K·D/s at N=10M,D=128,K=1024 diag; % tensor-core peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# dram__bytes_read.sum + dram__bytes_write.sum of one fused-kernel launch on the
+# full 10M x 128 workload: 307.8 MB measured on its first 1M rows, times 10
+TRAFFIC_EMBED_10M = 3.078e9
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -283,6 +286,13 @@ def run_ours(args, w, ws, rank, local):
     launches_per_step = max(1, main_launches // args.steps)
     achieved = flops / launches_per_step / (per_launch_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
+    # DRAM bytes per launch of the fused kernel from the committed ncu capture
+    # (1M rows of this workload, scaled by rows: traffic grows with N); only
+    # for the configuration that capture was taken of
+    traffic = None
+    if (w.name == "embed_10m" and args.plan in ("auto", "cluster") and args.precision == "auto"
+            and not args.rows):
+        traffic = TRAFFIC_EMBED_10M
     line = {
         "metric": METRIC, "value": ws * 1e3 / ms_max, "unit": "EM iter/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -290,7 +300,8 @@ def run_ours(args, w, ws, rank, local):
         "data": "synthetic", "config": config_of(w, args.precision, args.plan),
         "nkd_per_s": ws * w.N * w.K * w.D * 1e3 / ms_max,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "traffic_source": "ncu dram__bytes_read+write, 1M-row capture x 10" if traffic else None,
                      "kernel": "fused_em_kernel", "launch_ms": per_launch_ms,
                      "peak_source": f"{peaks_kind} bf16 burst (fp16 has the same nominal rate)",
                      "work": "8*N*K*D MMA flops per step"},
