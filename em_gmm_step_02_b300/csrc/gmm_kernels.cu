@@ -564,8 +564,7 @@ __device__ __forceinline__ void flush_stats(double* prow, uint32_t taddr, int h,
 //         the statistics MMA, and the periodic flush of the statistics.
 // Two receive slots are safe: a CTA pushes tile t only after its B(t-1),
 // which needs every CTA's push of t-1, which each makes only after its own
-// B(t-2) has read the slot that tile t reuses (and after the copies of
-// tile t-2 out of its own chunk had landed).
+// B(t-2) has read the slot that tile t reuses.
 // The two warps that share a lane quarter (one per column half) meet at a
 // named barrier of their own.
 template <typename CF>
@@ -648,22 +647,17 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
       const float tot = S->pair_s[0][nl] + S->pair_s[1][nl];
       lse_loc = tot > 0.f ? m + lg2(tot) - kLog2R : -CUDART_INF_F;
     }
-    // push this CTA's row normalisers of tile j to every other CTA of the
-    // cluster: each warp of column half 0 writes its 32 rows into its own
-    // chunk of the slot and one lane bulk-copies the 128-byte chunk to the
-    // same place in every peer (one transaction per chunk and peer)
-    if (exch && h == 0) {
-      if (lane == 0) bulk_wait_read_all();     // the previous copies have read the chunk
-      __syncwarp();
-      S->xrecv[j & 1][rank][nl] = lse_loc;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t src = smem_u32(&S->xrecv[j & 1][rank][32 * q]);
-        const uint32_t bar = smem_u32(&S->xready[j & 1]);
-        for (int r = 0; r < C; ++r)
-          if (r != rank) bulk_s2c(mapa(src, r), src, 128u, mapa(bar, r));
-        bulk_commit_group();
+    // push this CTA's row normalisers of tile j to every CTA of the cluster;
+    // both threads of a row hold the value and share the stores (ranks of
+    // their own parity); each store completes 4 transaction bytes on the
+    // destination's slot barrier
+    if (exch) {
+      const uint32_t dst = smem_u32(&S->xrecv[j & 1][rank][nl]);
+      const uint32_t bar = smem_u32(&S->xready[j & 1]);
+#pragma unroll
+      for (int r2 = 0; r2 < 4; ++r2) {
+        const int r = 2 * r2 + h;
+        if (r < C) st_async_f32(mapa(dst, r), lse_loc, mapa(bar, r));
       }
     }
     // ---------------------------------------------------------------- B(j): normalise, R tile
@@ -678,12 +672,11 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
         lse = valid ? __ldg(a.lse_in + pn) : -CUDART_INF_F;
       } else if (C > 1) {
         const int slot = jj & 1;
-        if (st == 0) mbar_arrive_expect_tx(&S->xready[slot], static_cast<uint32_t>((C - 1) * kBN * 4));
+        if (st == 0) mbar_arrive_expect_tx(&S->xready[slot], static_cast<uint32_t>(C * kBN * 4));
         mbar_wait(&S->xready[slot], (jj >> 1) & 1, abort_flag, a.status);
         float vals[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-          vals[r] = r == rank ? lse_loc : (r < C ? S->xrecv[slot][r][nl] : -CUDART_INF_F);
+        for (int r = 0; r < 8; ++r) vals[r] = r < C ? S->xrecv[slot][r][nl] : -CUDART_INF_F;
         float mx = vals[0];
 #pragma unroll
         for (int r = 1; r < 8; ++r) mx = fmaxf(mx, vals[r]);
