@@ -837,12 +837,19 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
   const uint32_t sOnes = smem_u32(sm + CF::kOffOnes);
   constexpr uint32_t kAbType = 0u;   // fp16 operands (PRECISE: hi and lo pieces)
 
+  // FAST EM: the softmax warps hold a tile's logits and responsibilities in
+  // registers; the transform warpgroup gives up 16 registers a thread so that
+  // the two softmax warpgroups get 8 more each (per SM sub-partition: one
+  // transform warp, two softmax warps, 512 registers moved either way).
+  constexpr bool kRegSplit = NP == 1 && !kTopm;
   if (warp < 4) {
     // ================================================= transform warps
+    if constexpr (kRegSplit) regs_release<112>();
     if (a.x_bf16) transform_warps<CF, NP, NCH, NST, true, kTopm>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
     else transform_warps<CF, NP, NCH, NST, false, kTopm>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
   } else if (warp < 12 && NP == 1 && !kTopm) {
     // ================================================= softmax warps (FAST EM)
+    if constexpr (kRegSplit) regs_claim<136>();
     softmax_fast<CF>(a, sm, S, abort_flag, tid, warp, lane, rank, C, tgroup, n_tgroups, my_tiles, acc1, acc2,
                      kbase, kvalid);
   } else if (warp < 12) {
