@@ -552,6 +552,23 @@ __device__ __forceinline__ void flush_stats(double* prow, uint32_t taddr, int h,
   }
 }
 
+// The R operand of the statistics MMA is a ring of two slots of 32 points:
+// the rows of lane quarter q of every tile go to slot q & 1, so each slot
+// serves two quarters per tile (q and q ^ 2).  Quarter q of tile j may write
+// once the MMA has read the slot's previous user: quarter q - 2 of tile j
+// (q >= 2) or quarter q + 2 of tile j - 1 (q < 2).  Each quarter has its
+// own pair of barriers (r_full[q]: its rows written; r_done[q]: its rows
+// read), one phase per tile.  A writer's previous wait on r_done[q ^ 2] saw
+// the phase before the one it waits for now, and the phase after needs this
+// quarter's own write, so the parity test cannot be fooled by a phase two
+// steps away.
+__device__ __forceinline__ bool r_slot_wait(Small* S, int q, int j, volatile uint32_t* abort_flag,
+                                            uint32_t* status) {
+  if (q >= 2) return mbar_wait(&S->r_done[q - 2], static_cast<uint32_t>(j & 1), abort_flag, status);
+  if (j > 0) return mbar_wait(&S->r_done[q + 2], static_cast<uint32_t>((j - 1) & 1), abort_flag, status);
+  return true;
+}
+
 // ============================================================== FAST softmax warps
 // The softmax warps of the FAST (single fp16 piece) EM, normaliser and
 // statistics-given modes.  Per tile:
@@ -576,7 +593,6 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
   const int q = warp & 3;                 // TMEM lane quarter
   const int h = (warp - 4) >> 2;          // column half
   const int nl = 32 * q + lane;           // point row inside the tile
-  const int rho = q >> 1;                 // statistics half this row belongs to
   const int pbar = 3 + q;                 // named barrier of the pair of warps of this quarter
   const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
   const bool given = a.mode == MODE_GIVEN;
@@ -667,10 +683,14 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
     {
       const int jj = j;
       const bool valid = pn < a.N;
+      const bool early_r = want_r && exch && q < 2 && jj > 0;
       float lse = plse;
       if (given) {
         lse = valid ? __ldg(a.lse_in + pn) : -CUDART_INF_F;
       } else if (C > 1) {
+        // quarters 0-1 wait for their R slot (freed by the previous tile's
+        // quarters 2-3) here, where the wait overlaps the exchange
+        if (early_r) r_slot_wait(S, q, jj, abort_flag, a.status);
         const int slot = jj & 1;
         if (st == 0) mbar_arrive_expect_tx(&S->xready[slot], static_cast<uint32_t>(C * kBN * 4));
         mbar_wait(&S->xready[slot], (jj >> 1) & 1, abort_flag, a.status);
@@ -699,24 +719,19 @@ __device__ __forceinline__ void softmax_fast(const FusedArgs& a, uint8_t* sm, Sm
           x = __hmul2(x, f2);
           pk[i] = *reinterpret_cast<uint32_t*>(&x);
         }
-        // the R buffer is free once the statistics MMA has read the previous
-        // half written into it: half 1 of tile jj-1 for rows 0-63, half 0 of
-        // tile jj for rows 64-127 (one barrier per half, one phase per tile)
-        if (rho == 0) {
-          if (jj > 0) mbar_wait(&S->r_done[1], (jj - 1) & 1, abort_flag, a.status);
-        } else {
-          mbar_wait(&S->r_done[0], jj & 1, abort_flag, a.status);
-        }
-        uint8_t* rbase = sm + CF::kOffR + h * 8192;
-        const int nr = nl - 64 * rho;
+        // this quarter's 32 rows go to R slot q & 1 once the statistics MMA
+        // has read the quarter two before (with an exchange, quarters 0-1
+        // have waited for that already)
+        if (!early_r) r_slot_wait(S, q, jj, abort_flag, a.status);
+        uint8_t* rbase = sm + CF::kOffR + h * 8192 + (q & 1) * kRSlotBytes;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint4 w;
           w.x = pk[4 * c]; w.y = pk[4 * c + 1]; w.z = pk[4 * c + 2]; w.w = pk[4 * c + 3];
-          *reinterpret_cast<uint4*>(rbase + sw128_off(nr, c)) = w;
+          *reinterpret_cast<uint4*>(rbase + sw128_off(lane, c)) = w;
         }
         fence_proxy_async_smem();
-        mbar_arrive(&S->r_full[rho]);
+        mbar_arrive(&S->r_full[q]);
         // statistics leave tensor memory at the end of a flush period
         if (((jj + 1) % a.flush_tiles == 0) || (jj + 1 == my_tiles)) {
           ll += static_cast<double>(llf);
@@ -794,10 +809,10 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     mbar_init(&S->p_full, 1);
     mbar_init(&S->acc1_full, 1);
     mbar_init(&S->acc1_empty, 256);
-    mbar_init(&S->r_full[0], 128);
-    mbar_init(&S->r_full[1], 128);
-    mbar_init(&S->r_done[0], 1);
-    mbar_init(&S->r_done[1], 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&S->r_full[q], 64);
+      mbar_init(&S->r_done[q], 1);
+    }
     mbar_init(&S->acc2_full, 1);
     mbar_init(&S->acc2_empty, 256);
     mbar_init(&S->drain, 1);
@@ -858,7 +873,6 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     const int q = warp & 3;              // TMEM lane quarter
     const int h = (warp - 4) >> 2;       // column half
     const int nl = 32 * q + lane;        // point row inside the tile
-    const int rho = q >> 1;              // statistics half this row belongs to
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     double ll = 0.0;
     float llf = 0.f;              // fp32 part of ll, moved into ll at every flush
@@ -977,16 +991,11 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       // out of the fp16 subnormal range; finalize divides the statistics back.
       const float rscale = kRScale<NP>();
       const float f = (valid && lse > -CUDART_INF_F && m > -CUDART_INF_F) ? ex2(m - lse) * rscale : 0.f;
-      // responsibilities of this half-row into the statistics operand
-      // the R buffer is free once the statistics MMA has read the previous half
-      // written into it (one barrier per half, one phase per tile)
-      if (rho == 0) {
-        if (j > 0) mbar_wait(&S->r_done[1], (j - 1) & 1, abort_flag, a.status);
-      } else {
-        mbar_wait(&S->r_done[0], j & 1, abort_flag, a.status);
-      }
-      const int nr = nl - 64 * rho;        // row inside the 64-point half
-      uint8_t* rbase = sm + CF::kOffR + h * 8192;
+      // responsibilities of this quarter's rows into R slot q & 1, once the
+      // statistics MMA has read the quarter two before
+      r_slot_wait(S, q, j, abort_flag, a.status);
+      const int nr = lane;                 // row inside the 32-point slot
+      uint8_t* rbase = sm + CF::kOffR + h * 8192 + (q & 1) * kRSlotBytes;
       if constexpr (NP == 1) {
         // fp16 pairs of r * kRScale: the R tile
         uint32_t rw[32];
@@ -999,7 +1008,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
           *reinterpret_cast<uint4*>(rbase + sw128_off(nr, c)) = w;
         }
         fence_proxy_async_smem();
-        mbar_arrive(&S->r_full[rho]);
+        mbar_arrive(&S->r_full[q]);
       } else {
 #pragma unroll
         for (int e = 0; e < 64; ++e) v[e] *= f;
@@ -1022,7 +1031,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
           *reinterpret_cast<uint4*>(rbase + CF::kRBytes + off) = w;
         }
         fence_proxy_async_smem();
-        mbar_arrive(&S->r_full[rho]);
+        mbar_arrive(&S->r_full[q]);
       }
       // statistics leave tensor memory at the end of a flush period
       const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
@@ -1137,34 +1146,36 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
             mbar_wait(&S->acc2_empty, (flush_idx - 1) & 1, abort_flag, a.status);
             tc_fence_after();
           }
-          for (int rho = 0; rho < 2; ++rho) {
-            mbar_wait(&S->r_full[rho], j & 1, abort_flag, a.status);
+          // one lane quarter (32 points, R slot q & 1) at a time
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t sRq = sR + (q & 1) * kRSlotBytes;
+            mbar_wait(&S->r_full[q], static_cast<uint32_t>(j & 1), abort_flag, a.status);
             tc_fence_after();
-            for (int kk = 0; kk < 4; ++kk) {
+            for (int kk = 0; kk < 2; ++kk) {
 #pragma unroll
               for (int pr = 0; pr < (NP == 1 ? 1 : 3); ++pr) {
                 const int prr = pr == 2 ? 1 : 0;   // responsibility piece
                 const int pf = pr == 1 ? 1 : 0;    // data piece
-                const uint64_t ad = sdesc_sw128(sR + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
-                const uint64_t bd = sdesc_sw128(stage + pf * CF::kPieceBytes + rho * 8192 + 2048 * kk,
+                const uint64_t ad = sdesc_sw128(sRq + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
+                const uint64_t bd = sdesc_sw128(stage + pf * CF::kPieceBytes + q * 4096 + 2048 * kk,
                                                 kChunkBytes, 1024);
                 mma_f16_ss(acc2, ad, bd, id2, fresh ? 0u : 1u);
                 fresh = false;
               }
-              // rows 16 (4 rho + kk) .. +15 of the stage are no longer needed
-              mma_commit(&S->empty_g[s][4 * rho + kk]);
+              // rows 16 (2 q + kk) .. +15 of the stage are no longer needed
+              mma_commit(&S->empty_g[s][2 * q + kk]);
             }
             // S0: responsibilities against an all-ones operand (the same fp16
             // values as S1 and S2, summed in fp32 by the tensor core)
-            bool fresh0 = (rho == 0) && (j % a.flush_tiles == 0);
+            bool fresh0 = (q == 0) && (j % a.flush_tiles == 0);
             for (int prr = 0; prr < NP; ++prr)
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = sdesc_sw128(sR + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
+              for (int kk = 0; kk < 2; ++kk) {
+                const uint64_t ad = sdesc_sw128(sRq + prr * CF::kRBytes + 2048 * kk, 8192, 1024);
                 const uint64_t bd = sdesc_sw128(sOnes, kChunkBytes, 1024);
                 mma_f16_ss(acc2 + 2 * CF::kDp, ad, bd, id0, fresh0 ? 0u : 1u);
                 fresh0 = false;
               }
-            mma_commit(&S->r_done[rho]);
+            mma_commit(&S->r_done[q]);
           }
           const bool flush = ((j + 1) % a.flush_tiles == 0) || (j + 1 == my_tiles);
           if (flush) {

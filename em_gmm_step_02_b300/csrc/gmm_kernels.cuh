@@ -89,8 +89,8 @@ struct Small {
   uint64_t p_full;
   uint64_t acc1_full;
   uint64_t acc1_empty;
-  uint64_t r_full[2];     // half rho of the R tile written (128 threads), one phase per tile
-  uint64_t r_done[2];     // half rho of the R tile read by the statistics MMA
+  uint64_t r_full[4];     // lane quarter q's rows written to R slot q & 1 (64 threads), one phase per tile
+  uint64_t r_done[4];     // lane quarter q's rows read by the statistics MMA
   uint64_t acc2_full;
   uint64_t acc2_empty;
   uint64_t xready[2];     // slot filled: every CTA of the cluster has pushed its row normalisers
@@ -114,7 +114,7 @@ struct Cfg {
   static constexpr int kOffP = NST * kStageBytes;
   static constexpr int kOffSmall = kOffP + NP * kPieceBytes;
   static constexpr int kOffR = (kOffSmall + static_cast<int>(sizeof(Small)) + 1023) / 1024 * 1024;
-  static constexpr int kRBytes = 64 * kSlice * 2;                     // 64 points x 128 comps x 16 bit
+  static constexpr int kRBytes = 2 * kRSlotBytes * 2;                // 2 slots x 32 points x 128 comps x 16 bit
   static constexpr int kOffOnes = kOffR + NP * kRBytes;             // 16 x 64 fp16 ones
   static constexpr int kEnd = kOffOnes + 2048;
   static constexpr int kDp = NCH * kAtomElems;

@@ -20,6 +20,7 @@ constexpr int kBN = 128;          // points per tile (tensor-core M of the logit
 constexpr int kSlice = 128;       // components per CTA
 constexpr int kAtomElems = 64;    // 16-bit elements per swizzled row
 constexpr int kChunkBytes = 128 * 128;  // one atom column of a 128-row tile
+constexpr int kRSlotBytes = 32 * 128;   // one R slot: 32 points x 64 components x 16 bit
 
 // Byte offset of the 16-byte chunk `c16` (0..7) of row `r` inside one atom column.
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c16) {
