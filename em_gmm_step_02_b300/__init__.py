@@ -59,6 +59,9 @@ def lib():
         L.gmm_em_step.restype = ctypes.c_int
         L.gmm_em_step_noalloc.argtypes = L.gmm_em_step.argtypes
         L.gmm_em_step_noalloc.restype = ctypes.c_int
+        L.gmm_em_step_host.argtypes = [vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, i64,
+                                       ctypes.POINTER(gmm_opts), vp]
+        L.gmm_em_step_host.restype = ctypes.c_int
         L.gmm_predict_topm.argtypes = [vp, i64, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp,
                                        ctypes.POINTER(gmm_opts), vp]
         L.gmm_predict_topm.restype = ctypes.c_int
@@ -164,6 +167,38 @@ def gmm_em_step(X, log_weights, means, vars_, cov="diag", *, out=None, opts: gmm
                            _dev(out[1], "new_means", torch.float32),
                            _dev(out[2], "new_vars", torch.float32),
                            _dev(ll, "total_loglik", torch.float64), ctypes.byref(opts), _stream(stream))
+    _check(rc)
+    return out[0], out[1], out[2], ll
+
+
+def gmm_em_step_host(X_host, log_weights, means, vars_, cov="diag", *, chunk_rows=0, out=None,
+                     opts: gmm_opts | None = None, stream=None, **opt_kw):
+    """One EM step over X held in host memory (see gmm_em_step_host in
+    include/gmm.h): the library copies X to the GPU in chunks of
+    ``chunk_rows`` rows (0: its default) while the previous chunk is being
+    processed.  X_host is a contiguous CPU tensor, best page-locked
+    (``pin_memory()``) so that the copies overlap the kernels; ``x_absmax``
+    (a bound on max |X|) must be given.  Parameters and outputs are CUDA
+    tensors, as for gmm_em_step."""
+    if not isinstance(X_host, torch.Tensor) or X_host.is_cuda:
+        raise TypeError("X_host must be a CPU tensor")
+    if not X_host.is_contiguous():
+        raise ValueError("X_host must be contiguous")
+    N, D, K, cov_i, dt = _shape(X_host, means, cov)
+    if opts is None:
+        opts = gmm_default_opts(**opt_kw)
+    if out is None:
+        out = (torch.empty_like(log_weights), torch.empty_like(means), torch.empty_like(vars_))
+    ll = torch.empty(1, dtype=torch.float64, device=means.device)
+    opts.loglik_on_host = 0
+    rc = lib().gmm_em_step_host(ctypes.c_void_p(X_host.data_ptr()), N, D, K, cov_i, dt,
+                                _dev(log_weights, "log_weights", torch.float32),
+                                _dev(means, "means", torch.float32), _dev(vars_, "vars", torch.float32),
+                                _dev(out[0], "new_log_weights", torch.float32),
+                                _dev(out[1], "new_means", torch.float32),
+                                _dev(out[2], "new_vars", torch.float32),
+                                _dev(ll, "total_loglik", torch.float64), int(chunk_rows), ctypes.byref(opts),
+                                _stream(stream))
     _check(rc)
     return out[0], out[1], out[2], ll
 

@@ -66,6 +66,8 @@ struct Plan {
 };
 
 constexpr int kCombineBlocks = 296;
+// default rows per chunk of the host-data entry point (1 GiB of bf16 rows at D = 128)
+constexpr int64_t kHostChunkRows = int64_t(1) << 22;
 constexpr size_t kStatusBytes = 256;
 
 int device_sms() {
@@ -367,6 +369,97 @@ FusedArgs base_args(const Plan& p, const void* X, uint8_t* ws) {
   return a;
 }
 
+// E-step kernels over the rows a.X[0, p.N): the fused kernel (one pass), or
+// normaliser pass + combine + statistics pass.  The statistics add into the
+// partials at a.part (zeroed by the caller once per EM step); the
+// log-likelihood partials go to ll_part, *n_ll of them.
+int run_estep(const Plan& p, const FusedArgs& a, uint8_t* ws, double* ll_part, cudaStream_t s, int* n_ll) {
+  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  int r;
+  if (!p.two_pass) {
+    FusedArgs a0 = a;
+    a0.mode = MODE_EM;
+    a0.C = p.C;
+    a0.ll_part = ll_part;
+    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), p.smem, s, p.C, a0))) return r;
+    *n_ll = p.tg * p.C;   // one log-likelihood partial per CTA
+  } else {
+    // pass 1: per-point normaliser over each group of 1024 components
+    FusedArgs a1 = a;
+    a1.mode = MODE_LSE;
+    a1.C = p.C1;
+    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), p.smem, s, p.C1, a1))) return r;
+    float* lse = reinterpret_cast<float*>(ws + p.off_lse);
+    if ((r = launch(kernel_handle(K_LSE_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
+                    static_cast<const float*>(a.lse_part), p.n_kgroups, p.N, lse, ll_part)))
+      return r;
+    *n_ll = kCombineBlocks;
+    // pass 2: statistics of every slice given the normaliser
+    FusedArgs a2 = a;
+    a2.mode = MODE_GIVEN;
+    a2.C = 1;
+    a2.ll_part = nullptr;
+    if ((r = launch_main(fn, dim3(p.n_slices, p.tg), dim3(416), p.smem, s, 1, a2))) return r;
+  }
+  return GMM_OK;
+}
+
+// M-step from the partials of N_total points, and the total log-likelihood
+// (device pointer ll_dev); with loglik_on_host, the copy to the host, the
+// wait for the stream and the device status.
+int run_finalize(const Plan& p, int64_t N_total, uint8_t* ws, const double* ll_part, int n_ll,
+                 const gmm_opts& o, const float* means, const float* vars, float* new_log_weights,
+                 float* new_means, float* new_vars, double* total_loglik, cudaStream_t s) {
+  double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
+  float reg = o.reg_covar, floor_ = o.var_floor;
+  int Dp = p.nch * kAtomElems;
+  int r = launch(kernel_handle(K_FINALIZE), dim3(p.K), dim3(128), 0, s, 1,
+                 static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_part)), p.tg, p.K_pad, p.F, Dp,
+                 p.D, p.K, N_total, p.cov_diag, reg, floor_,
+                 static_cast<double>(p.fast ? kRScale<1>() : kRScale<2>()),
+                 static_cast<const Meta*>(reinterpret_cast<Meta*>(ws + p.off_meta)), ll_part, n_ll,
+                 new_log_weights, new_means, new_vars, means, vars, ll_dev);
+  if (r) return r;
+  if (o.loglik_on_host) {
+    CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    uint32_t st[2] = {0, 0};
+    CUDA_TRY(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
+    if (st[0]) {
+      CUDA_TRY(cudaMemset(ws, 0, sizeof(st)));
+      return status_to_code(st[0], st[1]);
+    }
+  }
+  return GMM_OK;
+}
+
+// Copy stream and events of the host-data entry point, one set per device.
+struct HostPipe {
+  cudaStream_t copy = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t copied[2] = {nullptr, nullptr};
+  cudaEvent_t freed[2] = {nullptr, nullptr};
+};
+std::mutex g_pipe_mu;
+std::map<int, HostPipe> g_pipes;
+
+int get_pipe(HostPipe** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe& hp = g_pipes[dev];
+  if (!hp.copy) {
+    CUDA_TRY(cudaStreamCreateWithFlags(&hp.copy, cudaStreamNonBlocking));
+    CUDA_TRY(cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming));
+    for (int b = 0; b < 2; ++b) {
+      CUDA_TRY(cudaEventCreateWithFlags(&hp.copied[b], cudaEventDisableTiming));
+      CUDA_TRY(cudaEventCreateWithFlags(&hp.freed[b], cudaEventDisableTiming));
+    }
+  }
+  *out = &hp;
+  return GMM_OK;
+}
+
 }  // namespace
 
 // ====================================================================== ABI
@@ -436,51 +529,82 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
   CUDA_TRY(cudaMemsetAsync(ws + p.off_part, 0, sizeof(double) * static_cast<size_t>(p.tg) * p.K_pad * p.F, s));
 
   FusedArgs a = base_args(p, X, ws);
-  int n_ll = p.tg * p.C;   // one log-likelihood partial per CTA
-  if (!p.two_pass) {
-    a.mode = MODE_EM;
-    a.C = p.C;
-    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), p.smem, s, p.C, a))) return r;
-  } else {
-    // pass 1: per-point normaliser over each group of 1024 components
-    FusedArgs a1 = a;
-    a1.mode = MODE_LSE;
-    a1.C = p.C1;
-    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), p.smem, s, p.C1, a1))) return r;
-    float* lse = reinterpret_cast<float*>(ws + p.off_lse);
-    if ((r = launch(kernel_handle(K_LSE_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
-                    static_cast<const float*>(a.lse_part), p.n_kgroups, p.N, lse,
-                    reinterpret_cast<double*>(ws + p.off_llpart))))
-      return r;
-    n_ll = kCombineBlocks;
-    // pass 2: statistics of every slice given the normaliser
-    FusedArgs a2 = a;
-    a2.mode = MODE_GIVEN;
-    a2.C = 1;
-    a2.ll_part = nullptr;
-    if ((r = launch_main(fn, dim3(p.n_slices, p.tg), dim3(416), p.smem, s, 1, a2))) return r;
+  double* ll_part = reinterpret_cast<double*>(ws + p.off_llpart);
+  int n_ll = 0;
+  if ((r = run_estep(p, a, ws, ll_part, s, &n_ll))) return r;
+  return run_finalize(p, p.N, ws, ll_part, n_ll, o, means, vars, new_log_weights, new_means, new_vars,
+                      total_loglik, s);
+}
+
+int gmm_em_step_host(const void* X_host, int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
+                     const float* log_weights, const float* means, const float* vars, float* new_log_weights,
+                     float* new_means, float* new_vars, double* total_loglik, int64_t chunk_rows,
+                     const gmm_opts* opts, void* stream) {
+  g_launches = 0;
+  gmm_opts o;
+  gmm_default_opts(&o);
+  if (opts) o = *opts;
+  if (!X_host) return fail(GMM_ERR_INVALID_ARG, "X_host is NULL");
+  if (!(o.x_absmax > 0.f))
+    return fail(GMM_ERR_INVALID_ARG, "gmm_em_step_host needs opts->x_absmax > 0 (a bound on max |X|)");
+  if (N < 1) return fail(GMM_ERR_INVALID_ARG, "N must be >= 1");
+  if (chunk_rows < 0) return fail(GMM_ERR_INVALID_ARG, "chunk_rows must be >= 0");
+  int r;
+  if ((r = check_ptr(log_weights, "log_weights")) || (r = check_ptr(means, "means")) ||
+      (r = check_ptr(vars, "vars")) || (r = check_ptr(new_log_weights, "new_log_weights")) ||
+      (r = check_ptr(new_means, "new_means")) || (r = check_ptr(new_vars, "new_vars")))
+    return r;
+  if (!total_loglik) return fail(GMM_ERR_INVALID_ARG, "total_loglik is NULL");
+  if (chunk_rows == 0) chunk_rows = kHostChunkRows;
+  // whole tiles per chunk, so that every chunk's rows start a tile
+  chunk_rows = std::max<int64_t>(kBN, chunk_rows / kBN * kBN);
+  const int64_t rows = std::min(chunk_rows, N);
+  const int64_t n_chunks = (N + rows - 1) / rows;
+  Plan p;   // planned for one chunk; the M-step uses all N rows
+  if ((r = make_plan(p, nullptr, rows, D, K, cov_type, x_dtype, o, true))) return r;
+  const size_t row_bytes = static_cast<size_t>(D) * (p.x_bf16 ? 2 : 4);
+  const size_t stage_bytes = align256(static_cast<size_t>(rows) * row_bytes);
+  const int n_ll_chunk = p.two_pass ? kCombineBlocks : p.tg * p.C;
+  const size_t off_ll_all = p.ws_bytes;
+  const size_t off_stage = off_ll_all + align256(sizeof(double) * static_cast<size_t>(n_chunks) * n_ll_chunk);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = nullptr;
+  if ((r = get_workspace(off_stage + 2 * stage_bytes, &ws))) return r;
+  HostPipe* hp = nullptr;
+  if ((r = get_pipe(&hp))) return r;
+  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  if ((r = set_smem_attr(fn, p.smem))) return r;
+
+  // the copies may overwrite the staging buffers only once the work already
+  // on the stream (an earlier call's kernels) is done
+  CUDA_TRY(cudaEventRecord(hp->start, s));
+  CUDA_TRY(cudaStreamWaitEvent(hp->copy, hp->start, 0));
+  if ((r = run_prep(p, nullptr, log_weights, means, vars, o, ws, s))) return r;
+  CUDA_TRY(cudaMemsetAsync(ws + p.off_part, 0, sizeof(double) * static_cast<size_t>(p.tg) * p.K_pad * p.F, s));
+  double* ll_all = reinterpret_cast<double*>(ws + off_ll_all);
+  CUDA_TRY(cudaMemsetAsync(ll_all, 0, sizeof(double) * static_cast<size_t>(n_chunks) * n_ll_chunk, s));
+  const uint8_t* src = static_cast<const uint8_t*>(X_host);
+  for (int64_t c = 0; c < n_chunks; ++c) {
+    const int b = static_cast<int>(c & 1);
+    const int64_t r0 = c * rows;
+    const int64_t nc = std::min(rows, N - r0);
+    uint8_t* stage = ws + off_stage + b * stage_bytes;
+    // chunk c reuses the buffer of chunk c - 2 once its kernels are done
+    if (c >= 2) CUDA_TRY(cudaStreamWaitEvent(hp->copy, hp->freed[b], 0));
+    CUDA_TRY(cudaMemcpyAsync(stage, src + static_cast<size_t>(r0) * row_bytes, static_cast<size_t>(nc) * row_bytes,
+                             cudaMemcpyHostToDevice, hp->copy));
+    CUDA_TRY(cudaEventRecord(hp->copied[b], hp->copy));
+    CUDA_TRY(cudaStreamWaitEvent(s, hp->copied[b], 0));
+    Plan pc = p;
+    pc.N = nc;
+    pc.n_tiles = static_cast<int>((nc + kBN - 1) / kBN);
+    FusedArgs a = base_args(pc, stage, ws);
+    int n_ll = 0;
+    if ((r = run_estep(pc, a, ws, ll_all + c * n_ll_chunk, s, &n_ll))) return r;
+    CUDA_TRY(cudaEventRecord(hp->freed[b], s));
   }
-  double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
-  {
-    float reg = o.reg_covar, floor_ = o.var_floor;
-    int Dp = p.nch * kAtomElems;
-    if ((r = launch(kernel_handle(K_FINALIZE), dim3(p.K), dim3(128), 0, s, 1,
-                    static_cast<const double*>(a.part), p.tg, p.K_pad, p.F, Dp, p.D, p.K, p.N, p.cov_diag, reg,
-                    floor_, static_cast<double>(p.fast ? kRScale<1>() : kRScale<2>()), static_cast<const Meta*>(a.meta), reinterpret_cast<const double*>(ws + p.off_llpart),
-                    n_ll, new_log_weights, new_means, new_vars, means, vars, ll_dev)))
-      return r;
-  }
-  if (o.loglik_on_host) {
-    CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaStreamSynchronize(s));
-    uint32_t st[2] = {0, 0};
-    CUDA_TRY(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
-    if (st[0]) {
-      CUDA_TRY(cudaMemset(ws, 0, sizeof(st)));
-      return status_to_code(st[0], st[1]);
-    }
-  }
-  return GMM_OK;
+  return run_finalize(p, N, ws, ll_all, static_cast<int>(n_chunks * n_ll_chunk), o, means, vars, new_log_weights,
+                      new_means, new_vars, total_loglik, s);
 }
 
 int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
@@ -620,6 +744,22 @@ void gmm_release(void) {
     }
   }
   g_ws.clear();
+  std::lock_guard<std::mutex> lk2(g_pipe_mu);
+  for (auto& kv : g_pipes) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(kv.first);
+    HostPipe& hp = kv.second;
+    cudaStreamSynchronize(hp.copy);
+    for (int b = 0; b < 2; ++b) {
+      cudaEventDestroy(hp.copied[b]);
+      cudaEventDestroy(hp.freed[b]);
+    }
+    cudaEventDestroy(hp.start);
+    cudaStreamDestroy(hp.copy);
+    cudaSetDevice(cur);
+  }
+  g_pipes.clear();
 }
 
 }  // extern "C"

@@ -147,6 +147,34 @@ int gmm_predict_topm(const void *X, int64_t N, int32_t D, int32_t K, int32_t cov
                      double *total_loglik, const gmm_opts *opts, void *stream);
 
 /*
+ * gmm_em_step_host -- the same EM step as gmm_em_step for X held in HOST
+ * memory, possibly larger than the GPU's ("Flash-GMM", introduction and
+ * contributions: the kernel's memory does not grow with N, so the data set
+ * may exceed the device; streaming X in chunks is this library's way of
+ * feeding such a data set).
+ *  - X_host: row-major N x D (x_dtype), contiguous, in host memory; it should
+ *    be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to run
+ *    asynchronously.  Parameters and outputs are device pointers exactly as
+ *    for gmm_em_step; they may alias the same way.
+ *  - The rows go to the GPU in chunks of chunk_rows rows (rounded down to a
+ *    multiple of 128; 0 picks 4,194,304) through two device staging buffers:
+ *    chunk c + 1 is copied on an internal stream while chunk c is processed
+ *    on `stream`.  The statistics of all chunks add into the same partials,
+ *    so the result equals one gmm_em_step over all N rows up to the order of
+ *    the floating-point sums.
+ *  - opts->x_absmax > 0 is required: the FAST operand scale must be fixed
+ *    before the first chunk is seen (GMM_ERR_INVALID_ARG otherwise).
+ *  - The workspace grows by two staging buffers of chunk_rows rows.  The
+ *    host buffer must stay valid and unchanged until the stream has passed
+ *    this call.  Error behaviour as gmm_em_step.
+ */
+int gmm_em_step_host(const void *X_host, int64_t N, int32_t D, int32_t K, int32_t cov_type,
+                     int32_t x_dtype, const float *log_weights, const float *means,
+                     const float *vars, float *new_log_weights, float *new_means,
+                     float *new_vars, double *total_loglik, int64_t chunk_rows,
+                     const gmm_opts *opts, void *stream);
+
+/*
  * gmm_em_step_noalloc -- the same EM step as gmm_em_step, for callers that
  * cannot allocate device memory while they run: for example a process whose
  * device memory is handed out up front by its own allocator, or a code path

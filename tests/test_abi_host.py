@@ -43,6 +43,20 @@ def test_argument_errors_are_found_on_the_host(kw, code):
     assert G.gmm_last_error() != ""
 
 
+def test_host_stream_argument_errors_are_found_on_the_host():
+    vp = ctypes.c_void_p
+    lib = G.lib()
+
+    def call(X=0x1000, amax=1.0, chunk=0, N=100):
+        o = G.gmm_default_opts(x_absmax=amax)
+        return lib.gmm_em_step_host(vp(X), N, 8, 4, 1, 0, vp(0x2000), vp(0x2000), vp(0x2000), vp(0x2000),
+                                    vp(0x2000), vp(0x2000), vp(0x3000), chunk, ctypes.byref(o), vp(0))
+    assert call(X=0) == -1
+    assert call(amax=0.0) == -1 and "x_absmax" in G.gmm_last_error()
+    assert call(chunk=-5) == -1
+    assert call(N=0) == -1
+
+
 def test_bad_options_rejected():
     assert _call(opts=G.gmm_default_opts(precision=7)) == -1
     assert _call(opts=G.gmm_default_opts(reg_covar=-1.0)) == -1
