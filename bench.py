@@ -249,6 +249,24 @@ def run_ours(args, w, ws, rank, local):
                 "job_ms": w.iters * ms + t_ms,
                 "job": f"{w.iters} EM iterations + top-{w.topm}"}
 
+    # threshold multi-assignment (compressed rows) of the same final pass:
+    # pairs with r >= 1/(m+1), at most m per point, so nothing is cut by the cap
+    thresh = None
+    if w.topm > 0 and not args.no_topm:
+        tau = 1.0 / (w.topm + 1) + 1e-6
+        G.gmm_assign_threshold(X, *p, w.cov, tau=tau, max_per_point=w.topm, opts=opts)
+        torch.cuda.synchronize(dev)
+        assert G.gmm_stream_status() == 0, G.gmm_last_error()
+        reps = 3
+        e0.record(stream)
+        for _ in range(reps):
+            off, _, _ = G.gmm_assign_threshold(X, *p, w.cov, tau=tau, max_per_point=w.topm,
+                                               capacity=w.N * w.topm, opts=opts)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        thresh = {"tau": tau, "max_per_point": w.topm, "ms": e0.elapsed_time(e1) / reps,
+                  "entries": int(off[-1].item())}
+
     # end to end through the public API with host buffers: X streams from
     # pinned host memory in chunks whose copies overlap the fused kernel
     # (gmm_em_step_host); parameters go up and results come back every step
@@ -323,6 +341,8 @@ def run_ours(args, w, ws, rank, local):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if thresh is not None:
+        line["threshold"] = thresh
     if topm is not None:
         line["topm"] = topm
     if not args.no_cpu and ws == 1:

@@ -26,7 +26,8 @@ PREC = {"auto": 0, "fast": 1, "precise": 2}
 PLAN = {"auto": 0, "cluster": 1, "split": 2}
 COV = {"spherical": SPHERICAL, "diag": DIAG}
 STATUS = {0: "GMM_OK", -1: "GMM_ERR_INVALID_ARG", -2: "GMM_ERR_UNSUPPORTED",
-          -3: "GMM_ERR_NONFINITE", -4: "GMM_ERR_CUDA", -5: "GMM_ERR_TIMEOUT", -6: "GMM_ERR_RANGE"}
+          -3: "GMM_ERR_NONFINITE", -4: "GMM_ERR_CUDA", -5: "GMM_ERR_TIMEOUT", -6: "GMM_ERR_RANGE",
+          -7: "GMM_ERR_CAPACITY"}
 
 
 class GmmError(RuntimeError):
@@ -62,6 +63,9 @@ def lib():
         L.gmm_em_step_host.argtypes = [vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, i64,
                                        ctypes.POINTER(gmm_opts), vp]
         L.gmm_em_step_host.restype = ctypes.c_int
+        L.gmm_assign_threshold.argtypes = [vp, i64, i32, i32, i32, i32, vp, vp, vp, ctypes.c_float, i32,
+                                           vp, vp, vp, i64, ctypes.POINTER(gmm_opts), vp]
+        L.gmm_assign_threshold.restype = ctypes.c_int
         L.gmm_predict_topm.argtypes = [vp, i64, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp,
                                        ctypes.POINTER(gmm_opts), vp]
         L.gmm_predict_topm.restype = ctypes.c_int
@@ -169,6 +173,34 @@ def gmm_em_step(X, log_weights, means, vars_, cov="diag", *, out=None, opts: gmm
                            _dev(ll, "total_loglik", torch.float64), ctypes.byref(opts), _stream(stream))
     _check(rc)
     return out[0], out[1], out[2], ll
+
+
+def gmm_assign_threshold(X, log_weights, means, vars_, cov="diag", *, tau, max_per_point=16,
+                         capacity=None, opts: gmm_opts | None = None, stream=None, **opt_kw):
+    """Threshold multi-assignment as compressed rows (see include/gmm.h):
+    returns (offsets (N+1) int64, idx int32, resp float32), CUDA tensors;
+    point i's entries are idx/resp[offsets[i]:offsets[i+1]].  With
+    ``capacity`` None the output is sized for the worst case
+    (N * max_per_point entries) and trimmed to the total."""
+    N, D, K, cov_i, dt = _shape(X, means, cov)
+    if opts is None:
+        opts = gmm_default_opts(**opt_kw)
+    cap = N * max_per_point if capacity is None else int(capacity)
+    offsets = torch.empty(N + 1, dtype=torch.int64, device=X.device)
+    idx = torch.empty(max(cap, 1), dtype=torch.int32, device=X.device)
+    resp = torch.empty(max(cap, 1), dtype=torch.float32, device=X.device)
+    opts.loglik_on_host = 0
+    rc = lib().gmm_assign_threshold(_dev(X, "X"), N, D, K, cov_i, dt,
+                                    _dev(log_weights, "log_weights", torch.float32),
+                                    _dev(means, "means", torch.float32), _dev(vars_, "vars", torch.float32),
+                                    ctypes.c_float(tau), int(max_per_point), _dev(offsets, "offsets"),
+                                    _dev(idx, "idx_out"), _dev(resp, "resp_out"), cap, ctypes.byref(opts),
+                                    _stream(stream))
+    _check(rc)
+    if capacity is None:
+        total = int(offsets[N].item())
+        return offsets, idx[:total], resp[:total]
+    return offsets, idx, resp
 
 
 def gmm_em_step_host(X_host, log_weights, means, vars_, cov="diag", *, chunk_rows=0, out=None,

@@ -250,6 +250,8 @@ int status_to_code(uint32_t st, uint32_t where = 0) {
   }
   if (st & ST_NONFINITE) return fail(GMM_ERR_NONFINITE, "a parameter is not finite or a variance is not positive");
   if (st & ST_RANGE) return fail(GMM_ERR_RANGE, "data magnitude outside the FAST operand range");
+  if (st & ST_CAPACITY)
+    return fail(GMM_ERR_CAPACITY, "more threshold-assignment entries than the output capacity (count in offsets[N])");
   return GMM_OK;
 }
 
@@ -460,6 +462,73 @@ int get_pipe(HostPipe** out) {
   return GMM_OK;
 }
 
+// Wait for the stream and return (and clear) the device status.
+int sync_status(uint8_t* ws, cudaStream_t s) {
+  CUDA_TRY(cudaStreamSynchronize(s));
+  uint32_t st[2] = {0, 0};
+  CUDA_TRY(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
+  if (st[0]) {
+    CUDA_TRY(cudaMemset(ws, 0, sizeof(st)));
+    return status_to_code(st[0], st[1]);
+  }
+  return GMM_OK;
+}
+
+// Workspace of the top-m pass placed from byte `base` on: per-group
+// candidate lists of the K > 1024 plan.
+struct TopmSpace {
+  size_t off_gval, off_gidx, end;
+};
+TopmSpace topm_space(const Plan& p, int m, size_t base) {
+  TopmSpace t{base, base, base};
+  if (p.two_pass) {
+    const size_t lb = align256(sizeof(float) * static_cast<size_t>(p.n_kgroups) * p.N * m);
+    t.off_gidx = base + lb;
+    t.end = t.off_gidx + lb;
+  }
+  return t;
+}
+
+// The top-m pass over X: each point's m largest responsibilities and their
+// components into resp_out / idx_out (N x m, device); the total
+// log-likelihood into ll_dev when it is not NULL.
+int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_out, double* ll_dev, uint8_t* ws,
+             const TopmSpace& ts, cudaStream_t s) {
+  const int maxm = m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
+  const void* fn = fused_fn(p.np, p.nch, p.nst, true);
+  FusedArgs a = base_args(p, X, ws);
+  a.mode = MODE_TOPM;
+  a.topm = m;
+  a.topm_max = maxm;
+  int r;
+  // (the candidate lists live in the idle data stage / R area)
+  if (!p.two_pass) {
+    a.C = p.C;
+    a.topm_groups = 1;
+    a.topm_val = resp_out;
+    a.topm_idx = idx_out;
+    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), p.smem, s, p.C, a))) return r;
+    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
+                              static_cast<const double*>(a.ll_part), p.tg * p.C, ll_dev)))
+      return r;
+  } else {
+    a.C = p.C1;
+    a.topm_groups = p.n_kgroups;
+    a.topm_val = reinterpret_cast<float*>(ws + ts.off_gval);
+    a.topm_idx = reinterpret_cast<int32_t*>(ws + ts.off_gidx);
+    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), p.smem, s, p.C1, a))) return r;
+    if ((r = launch(kernel_handle(K_TOPM_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
+                    static_cast<const float*>(a.lse_part), static_cast<const float*>(a.topm_val),
+                    static_cast<const int32_t*>(a.topm_idx), p.n_kgroups, p.N, m, resp_out, idx_out,
+                    a.ll_part)))
+      return r;
+    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
+                              static_cast<const double*>(a.ll_part), kCombineBlocks, ll_dev)))
+      return r;
+  }
+  return GMM_OK;
+}
+
 }  // namespace
 
 // ====================================================================== ABI
@@ -624,61 +693,69 @@ int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov
   if (m > K) return fail(GMM_ERR_INVALID_ARG, "m must not exceed K");
   Plan p;
   if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
-  const int maxm = m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
-  const size_t smem = p.smem;   // the candidate lists live in the idle data stage / R area
-  // per-group candidate lists of the K > 1024 plan (after the EM workspace)
-  size_t off_gval = p.ws_bytes, off_gidx = p.ws_bytes, need = p.ws_bytes;
-  if (p.two_pass) {
-    const size_t lb = align256(sizeof(float) * static_cast<size_t>(p.n_kgroups) * N * m);
-    off_gidx = off_gval + lb;
-    need = off_gidx + lb;
-  }
+  TopmSpace ts = topm_space(p, m, p.ws_bytes);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = nullptr;
-  if ((r = get_workspace(need, &ws))) return r;
-  const void* fn = fused_fn(p.np, p.nch, p.nst, true);
-  if ((r = set_smem_attr(fn, smem))) return r;
+  if ((r = get_workspace(ts.end, &ws))) return r;
+  if ((r = set_smem_attr(fused_fn(p.np, p.nch, p.nst, true), p.smem))) return r;
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
-
-  FusedArgs a = base_args(p, X, ws);
-  a.mode = MODE_TOPM;
-  a.topm = m;
-  a.topm_max = maxm;
   double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
-  if (!p.two_pass) {
-    a.C = p.C;
-    a.topm_groups = 1;
-    a.topm_val = resp_out;
-    a.topm_idx = idx_out;
-    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), smem, s, p.C, a))) return r;
-    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
-                              static_cast<const double*>(a.ll_part), p.tg * p.C, ll_dev)))
-      return r;
-  } else {
-    a.C = p.C1;
-    a.topm_groups = p.n_kgroups;
-    a.topm_val = reinterpret_cast<float*>(ws + off_gval);
-    a.topm_idx = reinterpret_cast<int32_t*>(ws + off_gidx);
-    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), smem, s, p.C1, a))) return r;
-    if ((r = launch(kernel_handle(K_TOPM_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
-                    static_cast<const float*>(a.lse_part), static_cast<const float*>(a.topm_val),
-                    static_cast<const int32_t*>(a.topm_idx), p.n_kgroups, p.N, m, resp_out, idx_out,
-                    a.ll_part)))
-      return r;
-    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
-                              static_cast<const double*>(a.ll_part), kCombineBlocks, ll_dev)))
-      return r;
-  }
+  if ((r = run_topm(p, X, m, resp_out, idx_out, ll_dev, ws, ts, s))) return r;
   if (o.loglik_on_host) {
     CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaStreamSynchronize(s));
-    uint32_t st[2] = {0, 0};
-    CUDA_TRY(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
-    if (st[0]) {
-      CUDA_TRY(cudaMemset(ws, 0, sizeof(st)));
-      return status_to_code(st[0], st[1]);
-    }
+    return sync_status(ws, s);
   }
+  return GMM_OK;
+}
+
+int gmm_assign_threshold(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
+                         const float* log_weights, const float* means, const float* vars, float tau,
+                         int32_t max_per_point, int64_t* offsets, int32_t* idx_out, float* resp_out,
+                         int64_t capacity, const gmm_opts* opts, void* stream) {
+  g_launches = 0;
+  gmm_opts o;
+  gmm_default_opts(&o);
+  if (opts) o = *opts;
+  if (!X) return fail(GMM_ERR_INVALID_ARG, "X is NULL");
+  int r;
+  if ((r = check_ptr(log_weights, "log_weights")) || (r = check_ptr(means, "means")) ||
+      (r = check_ptr(vars, "vars")))
+    return r;
+  if (!offsets || (reinterpret_cast<uintptr_t>(offsets) & 7))
+    return fail(GMM_ERR_INVALID_ARG, "offsets must be a non-NULL 8-byte aligned device pointer");
+  if (capacity < 0) return fail(GMM_ERR_INVALID_ARG, "capacity must be >= 0");
+  if (capacity > 0 && ((r = check_ptr(idx_out, "idx_out")) || (r = check_ptr(resp_out, "resp_out")))) return r;
+  if (!(tau > 0.f && tau <= 1.f)) return fail(GMM_ERR_INVALID_ARG, "tau must be in (0, 1]");
+  if (max_per_point < 1 || max_per_point > 16) return fail(GMM_ERR_UNSUPPORTED, "max_per_point must be in [1, 16]");
+  if (max_per_point > K) return fail(GMM_ERR_INVALID_ARG, "max_per_point must not exceed K");
+  Plan p;
+  if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
+  const int m = max_per_point;
+  const int64_t n_blocks = (N + kThreshBlock - 1) / kThreshBlock;
+  // workspace: the EM workspace, the top-m lists of every point, block totals
+  const size_t off_r = p.ws_bytes;
+  const size_t off_i = off_r + align256(sizeof(float) * static_cast<size_t>(N) * m);
+  const size_t off_b = off_i + align256(sizeof(int32_t) * static_cast<size_t>(N) * m);
+  TopmSpace ts = topm_space(p, m, off_b + align256(sizeof(int64_t) * static_cast<size_t>(n_blocks + 1)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = nullptr;
+  if ((r = get_workspace(ts.end, &ws))) return r;
+  if ((r = set_smem_attr(fused_fn(p.np, p.nch, p.nst, true), p.smem))) return r;
+  if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
+  float* tr = reinterpret_cast<float*>(ws + off_r);
+  int32_t* ti = reinterpret_cast<int32_t*>(ws + off_i);
+  int64_t* bt = reinterpret_cast<int64_t*>(ws + off_b);
+  if ((r = run_topm(p, X, m, tr, ti, nullptr, ws, ts, s))) return r;
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  if ((r = launch(kernel_handle(K_THRESH_COUNT), dim3(static_cast<unsigned>(n_blocks)), dim3(kThreshBlock), 0, s, 1,
+                  static_cast<const float*>(tr), N, m, tau, offsets, bt)))
+    return r;
+  if ((r = launch(kernel_handle(K_THRESH_SCAN), dim3(1), dim3(1024), 0, s, 1, bt, n_blocks))) return r;
+  if ((r = launch(kernel_handle(K_THRESH_SCATTER), dim3(static_cast<unsigned>(n_blocks)), dim3(kThreshBlock), 0, s,
+                  1, static_cast<const float*>(tr), static_cast<const int32_t*>(ti), N, m, tau, offsets,
+                  static_cast<const int64_t*>(bt), n_blocks, idx_out, resp_out, capacity, status)))
+    return r;
+  if (o.loglik_on_host) return sync_status(ws, s);
   return GMM_OK;
 }
 

@@ -1370,6 +1370,91 @@ __global__ void finalize_kernel(const double* __restrict__ part, int n_parts, in
   }
 }
 
+// ============================================================== threshold assignment
+// The multi-assignment of "Flash-GMM" (conclusion; the posting-list use in
+// its IVF experiments): every (point, component) pair whose responsibility
+// reaches a threshold, as compressed rows.  Input: each point's m largest
+// responsibilities in descending order (ties: lower index first) from the
+// top-m pass.  Three kernels: per-point counts with a block-local exclusive
+// scan, a scan of the block totals, and the scatter of the kept entries.
+
+// cnt_i = number of j < m with resp[i][j] >= tau (a prefix of the sorted
+// row).  offsets[i] <- exclusive scan of cnt within the block;
+// block_tot[b] <- the block's total.
+__global__ void __launch_bounds__(kThreshBlock) thresh_count_kernel(const float* __restrict__ resp, int64_t N,
+                                                                   int m, float tau, int64_t* __restrict__ offsets,
+                                                                   int64_t* __restrict__ block_tot) {
+  __shared__ int32_t sc[kThreshBlock];
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreshBlock + threadIdx.x;
+  int c = 0;
+  if (i < N) {
+    const float* r = resp + i * m;
+    while (c < m && r[c] >= tau) ++c;
+  }
+  sc[threadIdx.x] = c;
+  __syncthreads();
+  // Hillis-Steele inclusive scan over the block
+  for (int o = 1; o < kThreshBlock; o <<= 1) {
+    const int v = threadIdx.x >= static_cast<unsigned>(o) ? sc[threadIdx.x - o] : 0;
+    __syncthreads();
+    sc[threadIdx.x] += v;
+    __syncthreads();
+  }
+  if (i < N) offsets[i] = sc[threadIdx.x] - c;
+  if (threadIdx.x == kThreshBlock - 1) block_tot[blockIdx.x] = sc[threadIdx.x];
+}
+
+// One block: block_tot[b] <- exclusive scan over b; block_tot[n_blocks] <- the
+// total.  Chunks of 1024 with a running carry.
+__global__ void __launch_bounds__(1024) thresh_scan_kernel(int64_t* __restrict__ block_tot, int64_t n_blocks) {
+  __shared__ int64_t sc[1024];
+  __shared__ int64_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int64_t base = 0; base < n_blocks; base += 1024) {
+    const int64_t b = base + threadIdx.x;
+    const int64_t v = b < n_blocks ? block_tot[b] : 0;
+    sc[threadIdx.x] = v;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+      const int64_t u = threadIdx.x >= static_cast<unsigned>(o) ? sc[threadIdx.x - o] : 0;
+      __syncthreads();
+      sc[threadIdx.x] += u;
+      __syncthreads();
+    }
+    if (b < n_blocks) block_tot[b] = carry + sc[threadIdx.x] - v;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry += sc[1023];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) block_tot[n_blocks] = carry;
+}
+
+// offsets[i] += its block's offset; offsets[N] = total; the kept entries go
+// to idx_out / resp_out[offsets[i] ...] when the total fits `capacity`,
+// otherwise nothing is written there and ST_CAPACITY is raised.
+__global__ void __launch_bounds__(kThreshBlock) thresh_scatter_kernel(
+    const float* __restrict__ resp, const int32_t* __restrict__ idx, int64_t N, int m, float tau,
+    int64_t* __restrict__ offsets, const int64_t* __restrict__ block_tot, int64_t n_blocks,
+    int32_t* __restrict__ idx_out, float* __restrict__ resp_out, int64_t capacity, uint32_t* status) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreshBlock + threadIdx.x;
+  const int64_t total = block_tot[n_blocks];
+  if (i == 0) {
+    offsets[N] = total;
+    if (total > capacity) atomicOr(status, ST_CAPACITY);
+  }
+  if (i >= N) return;
+  const int64_t off = offsets[i] + block_tot[blockIdx.x];
+  offsets[i] = off;
+  if (total > capacity) return;
+  const float* r = resp + i * m;
+  const int32_t* k = idx + i * m;
+  for (int j = 0; j < m && r[j] >= tau; ++j) {
+    idx_out[off + j] = k[j];
+    resp_out[off + j] = r[j];
+  }
+}
+
 // Host-side handles of the kernels (launched from gmm_api.cu).
 const void* kernel_handle(KernelId id) {
   switch (id) {
@@ -1388,6 +1473,9 @@ const void* kernel_handle(KernelId id) {
     case K_FINALIZE: return reinterpret_cast<const void*>(&finalize_kernel);
     case K_TOPM_COMBINE: return reinterpret_cast<const void*>(&topm_combine_kernel);
     case K_LL_TOTAL: return reinterpret_cast<const void*>(&ll_total_kernel);
+    case K_THRESH_COUNT: return reinterpret_cast<const void*>(&thresh_count_kernel);
+    case K_THRESH_SCAN: return reinterpret_cast<const void*>(&thresh_scan_kernel);
+    case K_THRESH_SCATTER: return reinterpret_cast<const void*>(&thresh_scatter_kernel);
   }
   return nullptr;
 }

@@ -20,6 +20,7 @@ enum : uint32_t {
   ST_TIMEOUT = 1u,
   ST_NONFINITE = 2u,
   ST_RANGE = 4u,
+  ST_CAPACITY = 8u,       // threshold assignment: more entries than the output holds
 };
 
 // Per-call scalars computed on the device before the main pass.
@@ -34,7 +35,11 @@ enum KernelId : int {
   K_ABSMAX, K_ABSMAX_VEC, K_META, K_PARAMS_FAST, K_PARAMS_PRECISE,
   K_FUSED_1_1_2, K_FUSED_1_2_2, K_FUSED_2_1_1, K_LSE_COMBINE, K_FINALIZE,
   K_TOPM_COMBINE, K_LL_TOTAL, K_TOPM_1_1_2, K_TOPM_1_2_2, K_TOPM_2_1_1,
+  K_THRESH_COUNT, K_THRESH_SCAN, K_THRESH_SCATTER,
 };
+
+// Threshold assignment: points per block of the count and scatter kernels.
+constexpr int kThreshBlock = 256;
 
 // Host-side handle of a kernel, for cudaLaunchKernelEx (argument order and
 // types as in gmm_kernels.cu).

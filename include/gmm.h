@@ -73,7 +73,8 @@ typedef enum {
     GMM_ERR_NONFINITE = -3,     /* a parameter is NaN/inf, or a variance <= 0 */
     GMM_ERR_CUDA = -4,          /* a CUDA runtime call failed */
     GMM_ERR_TIMEOUT = -5,       /* a device-side wait exceeded its bound */
-    GMM_ERR_RANGE = -6          /* data too large for the FAST operand range */
+    GMM_ERR_RANGE = -6,         /* data too large for the FAST operand range */
+    GMM_ERR_CAPACITY = -7       /* gmm_assign_threshold: more entries than the output holds */
 } gmm_status_t;
 
 /* Launch plan of one EM step (or top-m pass).
@@ -145,6 +146,30 @@ int gmm_predict_topm(const void *X, int64_t N, int32_t D, int32_t K, int32_t cov
                      int32_t x_dtype, const float *log_weights, const float *means,
                      const float *vars, int32_t m, float *resp_out, int32_t *idx_out,
                      double *total_loglik, const gmm_opts *opts, void *stream);
+
+/*
+ * Threshold multi-assignment ("Flash-GMM", conclusion: border vectors are
+ * assigned to several clusters using the responsibilities), as compressed
+ * rows for posting lists: every (point, component) pair whose responsibility
+ * reaches a threshold.
+ *   For every point i, the components k with r_ik >= tau among the point's
+ *   max_per_point largest responsibilities, in descending order of r (equal
+ *   values: lower k first).  When tau > 1 / (max_per_point + 1) this is every
+ *   k with r_ik >= tau, since the responsibilities of a point sum to one.
+ *   offsets (N + 1 int64, device): point i's entries are
+ *   [offsets[i], offsets[i+1]); offsets[N] is the total.  idx_out (int32) and
+ *   resp_out (float32), device, hold `capacity` entries.  If the total
+ *   exceeds capacity, offsets are still written, the entries are not, and
+ *   the device status reports GMM_ERR_CAPACITY (read offsets[N] and call
+ *   again with room for it).
+ * Supported: 0 < tau <= 1, 1 <= max_per_point <= min(K, 16); other limits
+ * as gmm_predict_topm.  The total log-likelihood is not computed.
+ */
+int gmm_assign_threshold(const void *X, int64_t N, int32_t D, int32_t K, int32_t cov_type,
+                         int32_t x_dtype, const float *log_weights, const float *means,
+                         const float *vars, float tau, int32_t max_per_point, int64_t *offsets,
+                         int32_t *idx_out, float *resp_out, int64_t capacity,
+                         const gmm_opts *opts, void *stream);
 
 /*
  * gmm_em_step_host -- the same EM step as gmm_em_step for X held in HOST

@@ -134,6 +134,23 @@ class Oracle:
         return r, idx, float(ll[0])
 
 
+def threshold_assign(r, tau, max_per_point):
+    """Threshold multi-assignment written from its definition: for every
+    point (row of the N x K responsibility matrix r), the components with
+    r >= tau in descending order of r (equal values: lower index first), at
+    most max_per_point of them; as compressed rows (offsets N+1, idx, resp)."""
+    r = np.asarray(r, np.float64)
+    offsets = [0]
+    idx, resp = [], []
+    for row in r:
+        order = sorted(range(len(row)), key=lambda k: (-row[k], k))
+        kept = [k for k in order if row[k] >= tau][:max_per_point]
+        idx.extend(kept)
+        resp.extend(row[k] for k in kept)
+        offsets.append(len(idx))
+    return np.array(offsets, np.int64), np.array(idx, np.int32), np.array(resp, np.float64)
+
+
 def _f32(a):
     return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
 

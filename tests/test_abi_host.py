@@ -57,6 +57,20 @@ def test_host_stream_argument_errors_are_found_on_the_host():
     assert call(N=0) == -1
 
 
+def test_threshold_assignment_argument_errors_are_found_on_the_host():
+    vp = ctypes.c_void_p
+    lib = G.lib()
+
+    def call(tau=0.3, m=4, off=0x4000, cap=10, K=8):
+        o = G.gmm_default_opts()
+        return lib.gmm_assign_threshold(vp(0x1000), 100, 8, K, 1, 0, vp(0x2000), vp(0x2000), vp(0x2000),
+                                        ctypes.c_float(tau), m, vp(off), vp(0x5000), vp(0x6000), cap,
+                                        ctypes.byref(o), vp(0))
+    assert call(tau=0.0) == -1 and call(tau=1.5) == -1 and call(tau=float("nan")) == -1
+    assert call(m=0) == -2 and call(m=17) == -2 and call(m=9, K=8) == -1
+    assert call(off=0) == -1 and call(off=0x4004) == -1 and call(cap=-1) == -1
+
+
 def test_bad_options_rejected():
     assert _call(opts=G.gmm_default_opts(precision=7)) == -1
     assert _call(opts=G.gmm_default_opts(reg_covar=-1.0)) == -1
