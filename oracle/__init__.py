@@ -134,6 +134,9 @@ class Oracle:
         return r, idx, float(ll[0])
 
 
+from . import tied  # noqa: E402  (tied-covariance EM, numpy)
+
+
 def threshold_assign(r, tau, max_per_point):
     """Threshold multi-assignment written from its definition: for every
     point (row of the N x K responsibility matrix r), the components with
