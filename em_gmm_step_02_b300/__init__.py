@@ -20,11 +20,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgmm_b300.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "gmm.h")
 
-SPHERICAL, DIAG = 0, 1
+SPHERICAL, DIAG, TIED = 0, 1, 2
 F32, BF16 = 0, 1
 PREC = {"auto": 0, "fast": 1, "precise": 2}
 PLAN = {"auto": 0, "cluster": 1, "split": 2}
-COV = {"spherical": SPHERICAL, "diag": DIAG}
+COV = {"spherical": SPHERICAL, "diag": DIAG, "tied": TIED}
 STATUS = {0: "GMM_OK", -1: "GMM_ERR_INVALID_ARG", -2: "GMM_ERR_UNSUPPORTED",
           -3: "GMM_ERR_NONFINITE", -4: "GMM_ERR_CUDA", -5: "GMM_ERR_TIMEOUT", -6: "GMM_ERR_RANGE",
           -7: "GMM_ERR_CAPACITY"}

@@ -61,6 +61,10 @@ struct Plan {
   size_t smem;
   // workspace offsets
   size_t off_meta, off_pimg, off_cadj, off_iscale, off_part, off_llpart, off_lsepart, off_lse, off_ll;
+  // tied covariance (cov_diag == 2): L, Sigma^-1, solve scratch, log|Sigma|, Gram
+  // matrix and its partials, per-component (N_k, nu_k), covariance scratch
+  size_t off_tl, off_sinv, off_twork, off_logdet, off_gram, off_gpart, off_tstats, off_tsig;
+  int n_gram;
   size_t n_llpart;
   size_t ws_bytes;
 };
@@ -143,7 +147,8 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   if (N < 1) return fail(GMM_ERR_INVALID_ARG, "N must be >= 1");
   if (D < 1) return fail(GMM_ERR_INVALID_ARG, "D must be >= 1");
   if (K < 1) return fail(GMM_ERR_INVALID_ARG, "K must be >= 1");
-  if (cov != GMM_SPHERICAL && cov != GMM_DIAG) return fail(GMM_ERR_INVALID_ARG, "cov_type must be 0 or 1");
+  if (cov != GMM_SPHERICAL && cov != GMM_DIAG && cov != GMM_TIED)
+    return fail(GMM_ERR_INVALID_ARG, "cov_type must be 0, 1 or 2");
   if (dtype != GMM_F32 && dtype != GMM_BF16) return fail(GMM_ERR_INVALID_ARG, "x_dtype must be 0 or 1");
   if (o.precision < GMM_PREC_AUTO || o.precision > GMM_PREC_PRECISE)
     return fail(GMM_ERR_INVALID_ARG, "unknown precision");
@@ -155,7 +160,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   if (K > 8192) return fail(GMM_ERR_UNSUPPORTED, "K > 8192 is not supported");
   if (N > (int64_t(1) << 40)) return fail(GMM_ERR_UNSUPPORTED, "N too large");
   if (X && (reinterpret_cast<uintptr_t>(X) & 15)) return fail(GMM_ERR_INVALID_ARG, "X must be 16-byte aligned");
-  p.N = N; p.D = D; p.K = K; p.cov_diag = cov == GMM_DIAG; p.x_bf16 = dtype == GMM_BF16;
+  p.N = N; p.D = D; p.K = K; p.cov_diag = cov; p.x_bf16 = dtype == GMM_BF16;
   const int prec = o.precision == GMM_PREC_AUTO ? (p.x_bf16 ? GMM_PREC_FAST : GMM_PREC_PRECISE) : o.precision;
   p.fast = prec == GMM_PREC_FAST;
   p.nch = D <= 64 ? 1 : 2;
@@ -204,6 +209,20 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
     off += align256(sizeof(float) * static_cast<size_t>(p.n_kgroups) * N);
     p.off_lse = off;
     off += align256(sizeof(float) * static_cast<size_t>(N));
+  }
+  p.n_gram = 0;
+  p.off_tl = p.off_sinv = p.off_twork = p.off_logdet = p.off_gram = p.off_gpart = p.off_tstats = p.off_tsig = off;
+  if (p.cov_diag == GMM_TIED) {
+    const size_t dd = sizeof(double) * static_cast<size_t>(D) * D;
+    p.n_gram = 2 * sms;
+    p.off_tl = off; off += align256(dd);
+    p.off_sinv = off; off += align256(dd);
+    p.off_twork = off; off += align256(dd);
+    p.off_logdet = off; off += 256;
+    p.off_gram = off; off += align256(dd);
+    p.off_gpart = off; off += align256(dd * p.n_gram);
+    p.off_tstats = off; off += align256(sizeof(double) * static_cast<size_t>(K) * (D + 1));
+    p.off_tsig = off; off += align256(sizeof(float) * static_cast<size_t>(D) * D);
   }
   p.ws_bytes = off;
   return GMM_OK;
@@ -338,14 +357,47 @@ int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, con
                    hint, meta, status);
     if (r) return r;
   }
+  const bool tied = p.cov_diag == GMM_TIED;
+  double* sinv = tied ? reinterpret_cast<double*>(ws + p.off_sinv) : nullptr;
+  double* logdet = tied ? reinterpret_cast<double*>(ws + p.off_logdet) : nullptr;
+  if (tied) {
+    // Sigma^-1 and log|Sigma| (one block), then the Gram matrix of the data
+    int r = launch(kernel_handle(K_TIED_PREP), dim3(1), dim3(128), 0, s, 1, var, p.D,
+                   reinterpret_cast<double*>(ws + p.off_tl), sinv, logdet,
+                   reinterpret_cast<double*>(ws + p.off_twork), status);
+    if (r) return r;
+    if (X) {
+      double* gpart = reinterpret_cast<double*>(ws + p.off_gpart);
+      r = launch(kernel_handle(p.x_bf16 ? K_GRAM_BF16 : K_GRAM_F32), dim3(p.n_gram, p.D > 64 ? 4 : 1), dim3(256),
+                 0, s, 1, X, p.N, p.D, static_cast<const Meta*>(meta), gpart);
+      if (r) return r;
+      r = launch(kernel_handle(K_GRAM_REDUCE), dim3((p.D * p.D + 255) / 256), dim3(256), 0, s, 1,
+                 static_cast<const double*>(gpart), p.n_gram, p.D, reinterpret_cast<double*>(ws + p.off_gram));
+      if (r) return r;
+    }
+  }
   {
     const void* fn = kernel_handle(p.fast ? K_PARAMS_FAST : K_PARAMS_PRECISE);
     int r = launch(fn, dim3(p.K_pad), dim3(128), 0, s, 1, lw, mu, var, p.D, p.K, p.cov_diag, p.nch,
                    static_cast<const Meta*>(meta), ws + p.off_pimg, reinterpret_cast<float*>(ws + p.off_cadj),
-                   reinterpret_cast<float*>(ws + p.off_iscale), status);
+                   reinterpret_cast<float*>(ws + p.off_iscale), status, static_cast<const double*>(sinv),
+                   static_cast<const double*>(logdet));
     if (r) return r;
   }
   return GMM_OK;
+}
+
+// Tied covariance, after the log-likelihood partials are summed into ll_dev:
+// the shared covariance of the M-step into new_vars (when not NULL; else into
+// scratch) and the per-point term -1/2 tr(Sigma^-1 G) into ll_dev.
+int run_tied_tail(const Plan& p, int K_stats, const gmm_opts& o, uint8_t* ws, float* new_vars, double* ll_dev,
+                  cudaStream_t s) {
+  float* out = new_vars ? new_vars : reinterpret_cast<float*>(ws + p.off_tsig);
+  return launch(kernel_handle(K_SIGMA_TIED), dim3(p.D), dim3(128), 0, s, 1,
+                static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_gram)),
+                static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_tstats)), K_stats, p.D, p.N,
+                o.reg_covar, o.var_floor, static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_sinv)),
+                ll_dev, out);
 }
 
 FusedArgs base_args(const Plan& p, const void* X, uint8_t* ws) {
@@ -420,8 +472,10 @@ int run_finalize(const Plan& p, int64_t N_total, uint8_t* ws, const double* ll_p
                  p.D, p.K, N_total, p.cov_diag, reg, floor_,
                  static_cast<double>(p.fast ? kRScale<1>() : kRScale<2>()),
                  static_cast<const Meta*>(reinterpret_cast<Meta*>(ws + p.off_meta)), ll_part, n_ll,
-                 new_log_weights, new_means, new_vars, means, vars, ll_dev);
+                 new_log_weights, new_means, new_vars, means, vars, ll_dev,
+                 p.cov_diag == GMM_TIED ? reinterpret_cast<double*>(ws + p.off_tstats) : nullptr);
   if (r) return r;
+  if (p.cov_diag == GMM_TIED && (r = run_tied_tail(p, p.K, o, ws, new_vars, ll_dev, s))) return r;
   if (o.loglik_on_host) {
     CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
     CUDA_TRY(cudaStreamSynchronize(s));
@@ -526,6 +580,12 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
                               static_cast<const double*>(a.ll_part), kCombineBlocks, ll_dev)))
       return r;
   }
+  if (ll_dev && p.cov_diag == GMM_TIED) {
+    // the logits' dropped per-point term, from the Gram matrix
+    gmm_opts d;
+    gmm_default_opts(&d);
+    if ((r = run_tied_tail(p, 0, d, ws, nullptr, ll_dev, s))) return r;
+  }
   return GMM_OK;
 }
 
@@ -616,6 +676,7 @@ int gmm_em_step_host(const void* X_host, int64_t N, int32_t D, int32_t K, int32_
   if (!X_host) return fail(GMM_ERR_INVALID_ARG, "X_host is NULL");
   if (!(o.x_absmax > 0.f))
     return fail(GMM_ERR_INVALID_ARG, "gmm_em_step_host needs opts->x_absmax > 0 (a bound on max |X|)");
+  if (cov_type == GMM_TIED) return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_host supports spherical and diagonal covariance");
   if (N < 1) return fail(GMM_ERR_INVALID_ARG, "N must be >= 1");
   if (chunk_rows < 0) return fail(GMM_ERR_INVALID_ARG, "chunk_rows must be >= 0");
   int r;
@@ -893,6 +954,7 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
       (r = check_ptr(new_means, "new_means")) || (r = check_ptr(new_vars, "new_vars")))
     return r;
   if (!total_loglik) return fail(GMM_ERR_INVALID_ARG, "total_loglik is NULL");
+  if (cov_type == GMM_TIED) return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_noalloc supports spherical and diagonal covariance");
   o.plan = GMM_PLAN_CLUSTER;   // the single pass: no N-sized buffer
   Plan p;
   if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
@@ -943,7 +1005,7 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
                     static_cast<const double*>(a.part), p.tg, p.K_pad, p.F, Dp, p.D, p.K, p.N, p.cov_diag, reg,
                     floor_, static_cast<double>(p.fast ? kRScale<1>() : kRScale<2>()), static_cast<const Meta*>(a.meta),
                     reinterpret_cast<const double*>(ws + p.off_llpart), p.tg * p.C, new_log_weights, new_means,
-                    new_vars, means, vars, ll_dev)))
+                    new_vars, means, vars, ll_dev, static_cast<double*>(nullptr))))
       return r;
   }
   if (o.loglik_on_host) {

@@ -169,12 +169,22 @@ __global__ void meta_kernel(const float* __restrict__ means, int D, int K, int u
 //   columns [Dp, Dp + D)  -1/(2 s2') * log2(e)     (x^2-part)
 // in the same swizzled K-major layout as the data tiles, and the logit
 // constant in log2 units.  x' = (x - shift) * scale, s2' = s2 * scale^2.
+//
+// Tied covariance (cov == 2; Sigma shared, its inverse `sinv` and log|Sigma|
+// from tied_prep_kernel): the logit drops its per-point term
+// -1/2 x'^T Sigma'^-1 x', which cancels in the responsibilities and is put
+// back into the log-likelihood from the data's Gram matrix, and keeps
+//   columns [0, D)        (Sigma^-1 (mu - shift))_d / scale * log2(e)
+//   columns [Dp, Dp + D)  0
+//   constant              (log pi - 1/2 (D log 2 pi + log|Sigma|
+//                          + (mu - shift)^T Sigma^-1 (mu - shift))) * log2(e)
 template <bool kFast>
 __global__ void params_kernel(const float* __restrict__ log_weights, const float* __restrict__ means,
                               const float* __restrict__ vars, int D, int K, int cov_diag, int nch,
                               const Meta* __restrict__ meta, uint8_t* __restrict__ p_img,
                               float* __restrict__ cadj, float* __restrict__ iscale,
-                              uint32_t* __restrict__ status) {
+                              uint32_t* __restrict__ status, const double* __restrict__ sinv,
+                              const double* __restrict__ tied_logdet) {
   const int k = blockIdx.x;
   const int d = threadIdx.x;   // blockDim.x == 128
   const int Dp = nch * kAtomElems;
@@ -183,7 +193,22 @@ __global__ void params_kernel(const float* __restrict__ log_weights, const float
   const bool valid_k = k < K;
   double b1 = 0.0, b2 = 0.0, cpart = 0.0;
   bool bad = false;
-  if (valid_k && d < D) {
+  __shared__ double nu[kMaxD];
+  if (cov_diag == 2) {
+    // tied: nu = mu_k - shift, then b1 = Sigma^-1 nu / scale
+    if (valid_k && d < D) {
+      const float mu = means[static_cast<int64_t>(k) * D + d];
+      bad = !isfinite(mu);
+      nu[d] = static_cast<double>(mu) - meta->shift[d];
+    }
+    __syncthreads();
+    if (valid_k && d < D) {
+      double w = 0.0;
+      for (int e = 0; e < D; ++e) w += sinv[static_cast<int64_t>(d) * D + e] * nu[e];
+      b1 = w / meta->scale * kLog2e;
+      cpart = nu[d] * w;
+    }
+  } else if (valid_k && d < D) {
     const float mu = means[static_cast<int64_t>(k) * D + d];
     const float v = cov_diag ? vars[static_cast<int64_t>(k) * D + d] : vars[k];
     bad = !isfinite(mu) || !isfinite(v) || !(v > 0.f);
@@ -215,7 +240,10 @@ __global__ void params_kernel(const float* __restrict__ log_weights, const float
     float lw = valid_k ? log_weights[k] : -CUDART_INF_F;
     if (valid_k && (lw != lw || lw == CUDART_INF_F)) atomicOr(status, ST_NONFINITE);
     float c = -CUDART_INF_F;
-    if (valid_k && lw > -CUDART_INF_F) c = static_cast<float>((static_cast<double>(lw) - 0.5 * red_c[0]) * kLog2e);
+    if (valid_k && lw > -CUDART_INF_F) {
+      const double q = cov_diag == 2 ? static_cast<double>(D) * kLog2Pi + *tied_logdet + red_c[0] : red_c[0];
+      c = static_cast<float>((static_cast<double>(lw) - 0.5 * q) * kLog2e);
+    }
     cadj[k] = c;
     iscale[k] = valid_k ? 1.f / s : 0.f;
   }
@@ -1313,7 +1341,8 @@ __global__ void finalize_kernel(const double* __restrict__ part, int n_parts, in
                                 const Meta* __restrict__ meta, const double* __restrict__ ll_part,
                                 int n_ll, float* __restrict__ out_lw, float* __restrict__ out_mu,
                                 float* __restrict__ out_var, const float* __restrict__ old_mu,
-                                const float* __restrict__ old_var, double* __restrict__ ll_out) {
+                                const float* __restrict__ old_var, double* __restrict__ ll_out,
+                                double* __restrict__ tied_stats) {
   const int k = blockIdx.x;
   const int d = threadIdx.x;
   __shared__ double red[128];
@@ -1326,7 +1355,7 @@ __global__ void finalize_kernel(const double* __restrict__ part, int n_parts, in
   float keep_mu = 0.f, keep_var = 0.f;
   if (d < D) {
     keep_mu = old_mu[static_cast<int64_t>(k) * D + d];
-    keep_var = cov_diag ? old_var[static_cast<int64_t>(k) * D + d] : old_var[k];
+    if (cov_diag != 2) keep_var = cov_diag ? old_var[static_cast<int64_t>(k) * D + d] : old_var[k];
   }
   __syncthreads();   // every old value is read before any output is written
   if (d < D) {
@@ -1344,12 +1373,18 @@ __global__ void finalize_kernel(const double* __restrict__ part, int n_parts, in
     vd = v;
     const double mu = m1 * isc + meta->shift[d];
     out_mu[static_cast<int64_t>(k) * D + d] = empty ? keep_mu : static_cast<float>(mu);
-    if (cov_diag) {
+    if (cov_diag == 2 && tied_stats) {
+      // tied: N_k and nu_k = mu_k - shift for the shared covariance (empty: 0)
+      double* ts = tied_stats + static_cast<int64_t>(k) * (D + 1);
+      if (d == 0) ts[0] = empty ? 0.0 : S0;
+      ts[1 + d] = empty ? 0.0 : m1 * isc;
+    }
+    if (cov_diag == 1) {
       const double vv = (v > var_floor ? v : static_cast<double>(var_floor)) + reg_covar;
       out_var[static_cast<int64_t>(k) * D + d] = empty ? keep_var : static_cast<float>(vv);
     }
   }
-  if (!cov_diag) {
+  if (cov_diag == 0) {
     red[d] = vd;
     __syncthreads();
     for (int o = 64; o > 0; o >>= 1) {
@@ -1367,6 +1402,188 @@ __global__ void finalize_kernel(const double* __restrict__ part, int n_parts, in
     double t = 0.0;
     for (int i = 0; i < n_ll; ++i) t += ll_part[i];
     *ll_out = t;
+  }
+}
+
+// ============================================================== tied covariance
+// One shared D x D covariance Sigma (the "tied" type of the "GMMXX" README's
+// "Covariance Coverage" table).  The E-step runs the fused kernel with the
+// linear logits of params_kernel (cov == 2); these kernels supply Sigma^-1
+// and log|Sigma|, the Gram matrix G = sum_i (x_i - shift)(x_i - shift)^T of
+// the data, and the M-step of the shared covariance:
+//   Sigma' = (G - sum_k N_k nu_k nu_k^T) / N,  nu_k = mu_k' - shift,
+// which is sum_k sum_i r_ik (x_i - mu_k')(x_i - mu_k')^T / N because the
+// responsibilities of a point sum to one; the dropped per-point term of the
+// logits returns to the log-likelihood as -1/2 tr(Sigma^-1 G).
+
+// One block of D threads, fp64 in global scratch: the Cholesky factor L of
+// Sigma (row-major, lower), log|Sigma|, and Sigma^-1 (thread j solves
+// L y = e_j, L^T x = y for column j).  A matrix that is not positive definite
+// (or not finite) raises ST_NONFINITE.
+__global__ void tied_prep_kernel(const float* __restrict__ sigma, int D, double* __restrict__ L,
+                                 double* __restrict__ sinv, double* __restrict__ logdet,
+                                 double* __restrict__ work, uint32_t* __restrict__ status) {
+  const int t = threadIdx.x;
+  __shared__ int bad;
+  if (t == 0) bad = 0;
+  __syncthreads();
+  for (int i = t; i < D * D; i += blockDim.x) {
+    const float v = sigma[i];
+    if (!isfinite(v)) bad = 1;
+    L[i] = v;
+  }
+  __syncthreads();
+  for (int j = 0; j < D; ++j) {
+    if (t == 0) {
+      double a = L[j * D + j];
+      for (int k = 0; k < j; ++k) a -= L[j * D + k] * L[j * D + k];
+      if (!(a > 0.0)) { bad = 1; a = 1.0; }
+      L[j * D + j] = sqrt(a);
+    }
+    __syncthreads();
+    for (int i = j + 1 + t; i < D; i += blockDim.x) {
+      double a = L[i * D + j];
+      for (int k = 0; k < j; ++k) a -= L[i * D + k] * L[j * D + k];
+      L[i * D + j] = a / L[j * D + j];
+    }
+    __syncthreads();
+  }
+  if (t == 0) {
+    double ld = 0.0;
+    for (int j = 0; j < D; ++j) ld += log(L[j * D + j]);
+    *logdet = 2.0 * ld;
+    if (bad) atomicOr(status, ST_NONFINITE);
+  }
+  // column t of Sigma^-1
+  for (int j = t; j < D; j += blockDim.x) {
+    double* y = work + static_cast<int64_t>(j) * D;
+    for (int i = 0; i < D; ++i) {
+      double a = i == j ? 1.0 : 0.0;
+      for (int k = 0; k < i; ++k) a -= L[i * D + k] * y[k];
+      y[i] = a / L[i * D + i];
+    }
+    for (int i = D - 1; i >= 0; --i) {
+      double a = y[i];
+      for (int k = i + 1; k < D; ++k) a -= L[k * D + i] * y[k];
+      y[i] = a / L[i * D + i];
+    }
+    for (int i = 0; i < D; ++i) sinv[static_cast<int64_t>(i) * D + j] = y[i];
+  }
+}
+
+// Gram matrix partials: block (bx, tile) accumulates the 64 x 64 tile `tile`
+// of G over rows bx, bx + gridDim.x, ... in chunks of 32 rows (fp32 within a
+// chunk, fp64 across chunks) and writes it to part[bx][D][D].  256 threads,
+// 4 x 4 outputs each.
+template <bool XB>
+__global__ void __launch_bounds__(256) gram_kernel(const void* __restrict__ X, int64_t N, int D,
+                                                   const Meta* __restrict__ meta, double* __restrict__ part) {
+  constexpr int R = 32;
+  __shared__ float As[R][64];
+  __shared__ float Bs[R][64];
+  const int ti = blockIdx.y >> 1, tj = blockIdx.y & 1;
+  const int i0 = 64 * ti, j0 = 64 * tj;
+  const int t = threadIdx.x;
+  const int ri = 4 * (t >> 4), cj = 4 * (t & 15);
+  double acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.0;
+  const int64_t n_chunks = (N + R - 1) / R;
+  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    __syncthreads();
+    for (int e = t; e < R * 64; e += 256) {
+      const int r = e >> 6, col = e & 63;
+      const int64_t n = c * R + r;
+      float va = 0.f, vb = 0.f;
+      if (n < N) {
+        if (i0 + col < D) {
+          const float x = XB ? __bfloat162float(static_cast<const __nv_bfloat16*>(X)[n * D + i0 + col])
+                             : static_cast<const float*>(X)[n * D + i0 + col];
+          va = x - meta->shift[i0 + col];
+        }
+        if (j0 + col < D) {
+          const float x = XB ? __bfloat162float(static_cast<const __nv_bfloat16*>(X)[n * D + j0 + col])
+                             : static_cast<const float*>(X)[n * D + j0 + col];
+          vb = x - meta->shift[j0 + col];
+        }
+      }
+      As[r][col] = va;
+      Bs[r][col] = vb;
+    }
+    __syncthreads();
+    float f[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) f[a][b] = 0.f;
+    for (int r = 0; r < R; ++r) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) av[a] = As[r][ri + a];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bv[b] = Bs[r][cj + b];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) f[a][b] = fmaf(av[a], bv[b], f[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] += static_cast<double>(f[a][b]);
+  }
+  double* out = part + static_cast<int64_t>(blockIdx.x) * D * D;
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int i = i0 + ri + a, j = j0 + cj + b;
+      if (i < D && j < D) out[static_cast<int64_t>(i) * D + j] = acc[a][b];
+    }
+}
+
+// G = sum over the partials, in a fixed order.
+__global__ void gram_reduce_kernel(const double* __restrict__ part, int n_parts, int D, double* __restrict__ G) {
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= static_cast<int64_t>(D) * D) return;
+  double s = 0.0;
+  for (int p = 0; p < n_parts; ++p) s += part[static_cast<int64_t>(p) * D * D + e];
+  G[e] = s;
+}
+
+// Shared covariance of the M-step (one block per row d, thread e = column):
+//   Sigma'_de = (G_de - sum_k N_k nu_kd nu_ke) / N, diagonal floored and
+//   regularised.  Block 0 also subtracts 1/2 tr(Sigma^-1 G) from the
+//   log-likelihood (the logits' dropped per-point term), when ll is given.
+__global__ void sigma_tied_kernel(const double* __restrict__ G, const double* __restrict__ tied_stats, int K,
+                                  int D, int64_t N, float reg_covar, float var_floor,
+                                  const double* __restrict__ sinv, double* __restrict__ ll,
+                                  float* __restrict__ out_sigma) {
+  const int d = blockIdx.x;
+  const int e = threadIdx.x;
+  if (e < D) {
+    double s = G[static_cast<int64_t>(d) * D + e];
+    for (int k = 0; k < K; ++k) {
+      const double* ts = tied_stats + static_cast<int64_t>(k) * (D + 1);
+      s -= ts[0] * ts[1 + d] * ts[1 + e];
+    }
+    s /= static_cast<double>(N);
+    if (d == e) s = (s > var_floor ? s : static_cast<double>(var_floor)) + reg_covar;
+    out_sigma[static_cast<int64_t>(d) * D + e] = static_cast<float>(s);
+  }
+  if (d == 0 && ll) {
+    __shared__ double red[128];
+    double t = 0.0;
+    for (int i = e; i < D * D; i += blockDim.x) t += sinv[i] * G[i];
+    red[e] = t;
+    __syncthreads();
+    if (e == 0) {
+      double tot = 0.0;
+      for (int i = 0; i < static_cast<int>(blockDim.x); ++i) tot += red[i];
+      *ll -= 0.5 * tot;
+    }
   }
 }
 
@@ -1476,6 +1693,11 @@ const void* kernel_handle(KernelId id) {
     case K_THRESH_COUNT: return reinterpret_cast<const void*>(&thresh_count_kernel);
     case K_THRESH_SCAN: return reinterpret_cast<const void*>(&thresh_scan_kernel);
     case K_THRESH_SCATTER: return reinterpret_cast<const void*>(&thresh_scatter_kernel);
+    case K_TIED_PREP: return reinterpret_cast<const void*>(&tied_prep_kernel);
+    case K_GRAM_BF16: return reinterpret_cast<const void*>(&gram_kernel<true>);
+    case K_GRAM_F32: return reinterpret_cast<const void*>(&gram_kernel<false>);
+    case K_GRAM_REDUCE: return reinterpret_cast<const void*>(&gram_reduce_kernel);
+    case K_SIGMA_TIED: return reinterpret_cast<const void*>(&sigma_tied_kernel);
   }
   return nullptr;
 }

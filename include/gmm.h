@@ -52,7 +52,13 @@
 extern "C" {
 #endif
 
-typedef enum { GMM_SPHERICAL = 0, GMM_DIAG = 1 } gmm_cov_t;
+/* Covariance types.  TIED: one full D x D covariance shared by all
+ * components ("GMMXX" README, "Covariance Coverage": tied, shape (D, D));
+ * vars / new_vars are then that D x D matrix (row-major, symmetric positive
+ * definite).  gmm_em_step, gmm_predict_topm and gmm_assign_threshold take
+ * all three; gmm_em_step_host and gmm_em_step_noalloc take SPHERICAL and
+ * DIAG. */
+typedef enum { GMM_SPHERICAL = 0, GMM_DIAG = 1, GMM_TIED = 2 } gmm_cov_t;
 typedef enum { GMM_F32 = 0, GMM_BF16 = 1 } gmm_dtype_t;
 
 /* Arithmetic of the two tensor-core contractions (logits and statistics).
@@ -112,7 +118,9 @@ void gmm_default_opts(gmm_opts *opts);
  *           new mean mu_k' = sum_i r_ik x_i / N_k;
  *           diagonal:  s2_kd' = sum_i r_ik (x_id - mu_kd')^2 / N_k
  *           spherical: s2_k'  = sum_i r_ik ||x_i - mu_k'||^2 / (D N_k)
- *           then s2' = max(s2', var_floor) + reg_covar.
+ *           tied:      Sigma' = sum_k sum_i r_ik (x_i - mu_k')(x_i - mu_k')^T / N
+ *           then s2' = max(s2', var_floor) + reg_covar (tied: on the
+ *           diagonal of Sigma').
  *   A component with N_k < 1e-30 keeps its mean and variance; its new
  *   log-weight is -inf.
  *   total_loglik = sum_i log sum_k pi_k N(x_i | mu_k, Sigma_k), evaluated at

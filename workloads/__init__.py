@@ -40,7 +40,7 @@ class Workload:
     N: int
     D: int
     K: int
-    cov: str          # "diag" | "spherical"
+    cov: str          # "diag" | "spherical" | "tied"
     x_dtype: str      # "f32" | "bf16"
     iters: int
     topm: int         # 0: no top-m pass
@@ -157,11 +157,12 @@ def _distinct_indices(N: int, K: int, g: torch.Generator) -> torch.Tensor:
 
 
 def make_init(w: Workload, X: torch.Tensor):
-    """Starting parameters (log_weights[K], means[K,D], vars[K] or [K,D]) as
-    float32 numpy arrays: means are K distinct random data points; variances are
-    1 for the tiny workload, else the per-dimension variance of the data
-    (over the first 2**20 rows; averaged over dimensions for a spherical
-    model); weights are uniform."""
+    """Starting parameters (log_weights[K], means[K,D], vars[K], [K,D] or, for
+    a tied model, the shared [D,D] covariance) as float32 numpy arrays: means
+    are K distinct random data points; variances are 1 for the tiny workload,
+    else the per-dimension variance of the data (over the first 2**20 rows;
+    averaged over dimensions for a spherical model; the data's covariance
+    matrix for a tied one); weights are uniform."""
     N, D, K = X.shape[0], w.D, w.K
     if N < K:
         raise ValueError(f"need at least K={K} rows to pick starting means, got {N}")
@@ -171,10 +172,14 @@ def make_init(w: Workload, X: torch.Tensor):
     means = X[idx.to(X.device)].float().cpu().numpy().astype(np.float32)
     if w.kind == "tiny":
         v = np.ones(D, np.float64)
+        cm = np.eye(D)
     else:
         sample = X[: min(N, CHUNK)].double().cpu().numpy()
         v = sample.var(axis=0)
-    if w.cov == "spherical":
+        cm = np.cov(sample.T, bias=True).reshape(D, D) if w.cov == "tied" else None
+    if w.cov == "tied":
+        vars_ = cm.astype(np.float32)
+    elif w.cov == "spherical":
         vars_ = np.full(K, v.mean(), np.float32)
     else:
         vars_ = np.tile(v.astype(np.float32), (K, 1))
