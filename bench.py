@@ -17,6 +17,7 @@ same workload per step and scales it to the full N (EM cost is linear in N).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -133,20 +134,25 @@ def max_over_ranks(ws, x: float) -> float:
     return float(t.item())
 
 
+def oracle_em_step(X, init, cov):
+    import oracle
+    if cov == "tied":
+        return oracle.tied.em_step(X.astype("float64"), *init)
+    return oracle.em_step(X, *init, cov)
+
+
 def oracle_rows_for(w, seconds: float, X_host_prefix, init, probe_rows=1000):
     """Rows of the workload the oracle handles in about `seconds`."""
-    import oracle
     probe = min(probe_rows, X_host_prefix.shape[0])
     t0 = time.perf_counter()
-    oracle.em_step(X_host_prefix[:probe], *init, w.cov)
+    oracle_em_step(X_host_prefix[:probe], init, w.cov)
     dt = max(time.perf_counter() - t0, 1e-3)
     return int(max(probe, min(X_host_prefix.shape[0], probe * seconds / dt)))
 
 
 def cpu_oracle_step(w, X_host, init, rows):
-    import oracle
     t0 = time.perf_counter()
-    oracle.em_step(X_host[:rows], *init, w.cov)
+    oracle_em_step(X_host[:rows], init, w.cov)
     return time.perf_counter() - t0
 
 
@@ -271,7 +277,7 @@ def run_ours(args, w, ws, rank, local):
     # pinned host memory in chunks whose copies overlap the fused kernel
     # (gmm_em_step_host); parameters go up and results come back every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and w.cov != "tied":      # the host-data entry point takes spherical / diagonal
         Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
         Xh.copy_(X)
         amax = float(X.abs().max().item()) * 1.0001    # the caller's bound on |X|, found once
@@ -372,10 +378,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-topm", action="store_true")
+    ap.add_argument("--cov", default=None, choices=["spherical", "diag", "tied"],
+                    help="run the workload's data with this covariance type instead")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-step-seconds", type=float, default=8.0)
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]
+    if args.cov and args.cov != w.cov:
+        w = dataclasses.replace(w, cov=args.cov, name=f"{w.name}_{args.cov}")
     if args.rows > 0:
         w = w.scaled(min(args.rows, w.N))
     ws, rank, local = dist_setup(args)
