@@ -1,6 +1,8 @@
 // gmm_api.cu -- host side of the C ABI declared in include/gmm.h: argument
 // checks, the launch plan (precision, cluster size, single or two-pass),
 // the per-device workspace, and the launch sequence of one EM step.
+#include <cublas_v2.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -70,6 +72,8 @@ struct Plan {
 };
 
 constexpr int kCombineBlocks = 296;
+// rows per chunk of the bf16 Gram matrix (one GEMM of the batch each)
+constexpr int64_t kGramRows = 8192;
 // default rows per chunk of the host-data entry point (1 GiB of bf16 rows at D = 128)
 constexpr int64_t kHostChunkRows = int64_t(1) << 22;
 constexpr size_t kStatusBytes = 256;
@@ -214,7 +218,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.off_tl = p.off_sinv = p.off_twork = p.off_logdet = p.off_gram = p.off_gpart = p.off_tstats = p.off_tsig = off;
   if (p.cov_diag == GMM_TIED) {
     const size_t dd = sizeof(double) * static_cast<size_t>(D) * D;
-    p.n_gram = 2 * sms;
+    p.n_gram = p.x_bf16 ? static_cast<int>((N + kGramRows - 1) / kGramRows) : 2 * sms;
     p.off_tl = off; off += align256(dd);
     p.off_sinv = off; off += align256(dd);
     p.off_twork = off; off += align256(dd);
@@ -326,6 +330,58 @@ int check_ptr(const void* p, const char* name) {
   return GMM_OK;
 }
 
+// cuBLAS handle per device (the Gram matrix of bf16 data is a plain GEMM).
+std::mutex g_blas_mu;
+std::map<int, cublasHandle_t> g_blas;
+
+int blas_handle(cublasHandle_t* out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_blas_mu);
+  cublasHandle_t& h = g_blas[dev];
+  if (!h && cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) {
+    h = nullptr;
+    return fail(GMM_ERR_CUDA, "cublasCreate failed");
+  }
+  *out = h;
+  return GMM_OK;
+}
+
+// part[b] = X_b^T X_b (D x D, fp32) for the row chunks X_b of kGramRows rows
+// of the row-major bf16 X: one strided batched GEMM (bf16 operands, fp32
+// accumulation) plus one GEMM for a shorter last chunk.  In column-major
+// terms X_b is the D x rows matrix A with leading dimension D, and
+// part[b] = A A^T.
+int gram_bf16(const Plan& p, const void* X, float* part, cudaStream_t s) {
+  cublasHandle_t h = nullptr;
+  int r = blas_handle(&h);
+  if (r) return r;
+  if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return fail(GMM_ERR_CUDA, "cublasSetStream failed");
+  const float one = 1.f, zero = 0.f;
+  const int D = p.D;
+  const int64_t full = p.N / kGramRows;
+  const int64_t rest = p.N - full * kGramRows;
+  const auto* x = static_cast<const __nv_bfloat16*>(X);
+  if (full > 0) {
+    cublasStatus_t st = cublasGemmStridedBatchedEx(
+        h, CUBLAS_OP_N, CUBLAS_OP_T, D, D, static_cast<int>(kGramRows), &one, x, CUDA_R_16BF, D,
+        kGramRows * D, x, CUDA_R_16BF, D, kGramRows * D, &zero, part, CUDA_R_32F, D,
+        static_cast<long long>(D) * D, static_cast<int>(full), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    if (st != CUBLAS_STATUS_SUCCESS) return fail(GMM_ERR_CUDA, "cublasGemmStridedBatchedEx failed");
+    ++g_launches;
+  }
+  if (rest > 0) {
+    const __nv_bfloat16* xr = x + full * kGramRows * D;
+    cublasStatus_t st = cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, D, D, static_cast<int>(rest), &one, xr,
+                                     CUDA_R_16BF, D, xr, CUDA_R_16BF, D, &zero,
+                                     part + full * static_cast<int64_t>(D) * D, CUDA_R_32F, D,
+                                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    if (st != CUBLAS_STATUS_SUCCESS) return fail(GMM_ERR_CUDA, "cublasGemmEx failed");
+    ++g_launches;
+  }
+  return GMM_OK;
+}
+
 // prep: scan (optional), meta, parameter images
 int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, const float* var,
              const gmm_opts& o, uint8_t* ws, cudaStream_t s) {
@@ -366,9 +422,16 @@ int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, con
                    reinterpret_cast<double*>(ws + p.off_tl), sinv, logdet,
                    reinterpret_cast<double*>(ws + p.off_twork), status);
     if (r) return r;
-    if (X) {
+    if (X && p.x_bf16) {
+      // bf16 data (FAST: unshifted) on the tensor cores, chunk by chunk
+      if ((r = gram_bf16(p, X, reinterpret_cast<float*>(ws + p.off_gpart), s))) return r;
+      r = launch(kernel_handle(K_GRAM_REDUCE_F32), dim3((p.D * p.D + 255) / 256), dim3(256), 0, s, 1,
+                 static_cast<const float*>(reinterpret_cast<float*>(ws + p.off_gpart)), p.n_gram, p.D,
+                 reinterpret_cast<double*>(ws + p.off_gram));
+      if (r) return r;
+    } else if (X) {
       double* gpart = reinterpret_cast<double*>(ws + p.off_gpart);
-      r = launch(kernel_handle(p.x_bf16 ? K_GRAM_BF16 : K_GRAM_F32), dim3(p.n_gram, p.D > 64 ? 4 : 1), dim3(256),
+      r = launch(kernel_handle(K_GRAM_F32), dim3(p.n_gram, p.D > 64 ? 4 : 1), dim3(256),
                  0, s, 1, X, p.N, p.D, static_cast<const Meta*>(meta), gpart);
       if (r) return r;
       r = launch(kernel_handle(K_GRAM_REDUCE), dim3((p.D * p.D + 255) / 256), dim3(256), 0, s, 1,
@@ -898,6 +961,15 @@ void gmm_release(void) {
     cudaSetDevice(cur);
   }
   g_pipes.clear();
+  std::lock_guard<std::mutex> lk3(g_blas_mu);
+  for (auto& kv : g_blas) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(kv.first);
+    if (kv.second) cublasDestroy(kv.second);
+    cudaSetDevice(cur);
+  }
+  g_blas.clear();
 }
 
 }  // extern "C"

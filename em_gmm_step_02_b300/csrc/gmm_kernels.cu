@@ -1544,6 +1544,16 @@ __global__ void __launch_bounds__(256) gram_kernel(const void* __restrict__ X, i
     }
 }
 
+// G = sum over float32 partials (the Gram matrices of row chunks from the
+// batched GEMM of bf16 data), in a fixed order, in fp64.
+__global__ void gram_reduce_f32_kernel(const float* __restrict__ part, int n_parts, int D, double* __restrict__ G) {
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= static_cast<int64_t>(D) * D) return;
+  double s = 0.0;
+  for (int p = 0; p < n_parts; ++p) s += static_cast<double>(part[static_cast<int64_t>(p) * D * D + e]);
+  G[e] = s;
+}
+
 // G = sum over the partials, in a fixed order.
 __global__ void gram_reduce_kernel(const double* __restrict__ part, int n_parts, int D, double* __restrict__ G) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -1697,6 +1707,7 @@ const void* kernel_handle(KernelId id) {
     case K_GRAM_BF16: return reinterpret_cast<const void*>(&gram_kernel<true>);
     case K_GRAM_F32: return reinterpret_cast<const void*>(&gram_kernel<false>);
     case K_GRAM_REDUCE: return reinterpret_cast<const void*>(&gram_reduce_kernel);
+    case K_GRAM_REDUCE_F32: return reinterpret_cast<const void*>(&gram_reduce_f32_kernel);
     case K_SIGMA_TIED: return reinterpret_cast<const void*>(&sigma_tied_kernel);
   }
   return nullptr;

@@ -36,7 +36,7 @@ enum KernelId : int {
   K_FUSED_1_1_2, K_FUSED_1_2_2, K_FUSED_2_1_1, K_LSE_COMBINE, K_FINALIZE,
   K_TOPM_COMBINE, K_LL_TOTAL, K_TOPM_1_1_2, K_TOPM_1_2_2, K_TOPM_2_1_1,
   K_THRESH_COUNT, K_THRESH_SCAN, K_THRESH_SCATTER,
-  K_TIED_PREP, K_GRAM_BF16, K_GRAM_F32, K_GRAM_REDUCE, K_SIGMA_TIED,
+  K_TIED_PREP, K_GRAM_BF16, K_GRAM_F32, K_GRAM_REDUCE, K_SIGMA_TIED, K_GRAM_REDUCE_F32,
 };
 
 // Threshold assignment: points per block of the count and scatter kernels.

@@ -28,7 +28,8 @@
  *    NULL = legacy default stream) and the call returns without waiting,
  *    unless opts->loglik_on_host is set.
  *  - The library keeps one internal workspace per device (O(K * D) bytes
- *    times the number of SMs, plus O(N) floats when K > 1024).  It is grown
+ *    times the number of SMs, plus O(N) floats when K > 1024, plus, for a
+ *    tied covariance of bf16 data, one D x D float matrix per 8192 rows).  It is grown
  *    on demand with cudaMalloc, so a call that needs a bigger workspace
  *    synchronises the device first; gmm_workspace_bytes() reports the size
  *    and gmm_reserve() allocates it up front.  Calls on different streams of
