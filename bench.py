@@ -59,7 +59,8 @@ class ClockSampler:
     def __init__(self, dev_index: int):
         self.dev = dev_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{dev_index}.csv")
+        out = os.environ.get("GMM_BENCH_CLOCKS_DIR", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out, f"clocks_rank{dev_index}.csv")
 
     def __enter__(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
