@@ -2,22 +2,26 @@
 restates its definition ("Flash-GMM", conclusion: border vectors assigned to
 several clusters from the responsibilities); these checks tie it to a
 hand-computed case with ties and to properties that follow from the
-responsibilities of a point summing to one."""
+responsibilities of a point summing to one.  Each pin also runs on copies of
+the function with a planted mistake, and every copy must fail one of them."""
+import inspect
+
 import numpy as np
+import pytest
 
 import oracle
 import workloads as W
 
 
-def test_hand_computed_case_with_ties():
+def pin_hand_computed_case_with_ties(fn):
     r = np.array([[0.5, 0.5, 0.0],
                   [0.2, 0.3, 0.5],
                   [0.1, 0.1, 0.8]])
-    off, idx, resp = oracle.threshold_assign(r, 0.3, 16)
+    off, idx, resp = fn(r, 0.3, 16)
     assert off.tolist() == [0, 2, 4, 5]
     assert idx.tolist() == [0, 1, 2, 1, 2]           # equal values: lower index first
     assert np.allclose(resp, [0.5, 0.5, 0.5, 0.3, 0.8])
-    off, idx, _ = oracle.threshold_assign(r, 0.3, 1)  # capped at one per point
+    off, idx, _ = fn(r, 0.3, 1)  # capped at one per point
     assert off.tolist() == [0, 1, 2, 3] and idx.tolist() == [0, 2, 2]
 
 
@@ -28,11 +32,11 @@ def _resp(seed=0, N=300, D=6, K=9):
     return oracle.responsibilities(X.numpy(), lw, mu, var, "diag")[0]
 
 
-def test_properties_on_real_responsibilities():
+def pin_properties_on_real_responsibilities(fn):
     r = _resp()
     N, K = r.shape
     for tau, m in ((0.05, 16), (0.2, 4), (0.34, 2), (0.6, 1)):
-        off, idx, resp = oracle.threshold_assign(r, tau, m)
+        off, idx, resp = fn(r, tau, m)
         assert off[0] == 0 and np.all(np.diff(off) >= 0) and off[-1] == len(idx)
         for i in range(N):
             ks = idx[off[i]:off[i + 1]]
@@ -43,9 +47,9 @@ def test_properties_on_real_responsibilities():
             assert np.allclose(resp[off[i]:off[i + 1]], r[i, ks])
 
 
-def test_tiny_threshold_gives_every_component_in_order():
+def pin_tiny_threshold_gives_every_component_in_order(fn):
     r = _resp(seed=1, N=50, K=7)
-    off, idx, _ = oracle.threshold_assign(r, 1e-300, 7)
+    off, idx, _ = fn(r, 1e-300, 7)
     kept = r >= 1e-300
     assert off[-1] == kept.sum()
     for i in range(len(r)):
@@ -54,12 +58,45 @@ def test_tiny_threshold_gives_every_component_in_order():
         assert ks.tolist() == order
 
 
-def test_threshold_above_one_half_keeps_the_argmax_or_nothing():
+def pin_threshold_above_one_half_keeps_the_argmax_or_nothing(fn):
     r = _resp(seed=2)
-    off, idx, _ = oracle.threshold_assign(r, 0.5 + 1e-9, 16)
+    off, idx, _ = fn(r, 0.5 + 1e-9, 16)
     for i in range(len(r)):
         ks = idx[off[i]:off[i + 1]]
         if r[i].max() >= 0.5 + 1e-9:
             assert ks.tolist() == [int(np.argmax(r[i]))]
         else:
             assert len(ks) == 0
+
+
+PINS = [pin_hand_computed_case_with_ties, pin_properties_on_real_responsibilities,
+        pin_tiny_threshold_gives_every_component_in_order, pin_threshold_above_one_half_keeps_the_argmax_or_nothing]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_threshold_oracle_pin(pin):
+    pin(oracle.threshold_assign)
+
+
+MUTANTS = {
+    "strict_threshold": ("if row[k] >= tau", "if row[k] > tau"),
+    "ties_to_higher_index": ("key=lambda k: (-row[k], k)", "key=lambda k: (-row[k], -k)"),
+    "ascending_order": ("key=lambda k: (-row[k], k)", "key=lambda k: (row[k], k)"),
+    "cap_ignored": ("[:max_per_point]", ""),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_threshold_mutant_is_caught(name):
+    old, new = MUTANTS[name]
+    src = inspect.getsource(oracle.threshold_assign)
+    assert src.count(old) == 1, name
+    ns = {"np": np}
+    exec(src.replace(old, new), ns)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(ns["threshold_assign"])
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches mutant {name}"
