@@ -71,6 +71,17 @@ def test_threshold_assignment_argument_errors_are_found_on_the_host():
     assert call(off=0) == -1 and call(off=0x4004) == -1 and call(cap=-1) == -1
 
 
+def test_tied_covariance_is_refused_where_not_supported():
+    vp = ctypes.c_void_p
+    lib = G.lib()
+    o = G.gmm_default_opts(x_absmax=1.0)
+    args = (vp(0x1000), 100, 8, 4, 2, 0, vp(0x2000), vp(0x2000), vp(0x2000), vp(0x2000), vp(0x2000),
+            vp(0x2000), vp(0x3000))
+    assert lib.gmm_em_step_host(*args, 0, ctypes.byref(o), vp(0)) == -2
+    assert lib.gmm_em_step_noalloc(*args, ctypes.byref(o), vp(0)) == -2
+    assert "spherical and diagonal" in G.gmm_last_error()
+
+
 def test_bad_options_rejected():
     assert _call(opts=G.gmm_default_opts(precision=7)) == -1
     assert _call(opts=G.gmm_default_opts(reg_covar=-1.0)) == -1
