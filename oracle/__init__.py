@@ -135,6 +135,7 @@ class Oracle:
 
 
 from . import tied  # noqa: E402  (tied-covariance EM, numpy)
+from . import topk_em  # noqa: E402  (approximate top-k EM, numpy)
 
 
 def threshold_assign(r, tau, max_per_point):
