@@ -122,8 +122,8 @@ void gmm_default_opts(gmm_opts *opts);
  *           tied:      Sigma' = sum_k sum_i r_ik (x_i - mu_k')(x_i - mu_k')^T / N
  *           then s2' = max(s2', var_floor) + reg_covar (tied: on the
  *           diagonal of Sigma').
- *   A component with N_k < 1e-30 keeps its mean and variance; its new
- *   log-weight is -inf.
+ *   A component with N_k < 1e-30 keeps its mean and variance (tied: its
+ *   mean; it adds nothing to Sigma'); its new log-weight is -inf.
  *   total_loglik = sum_i log sum_k pi_k N(x_i | mu_k, Sigma_k), evaluated at
  *   the INPUT parameters (a by-product of the E-step), as one double; a
  *   device pointer unless opts->loglik_on_host.
