@@ -71,7 +71,9 @@ def test_threshold_against_oracle(N, D, K, cov, xd, tau, m):
 
 @pytest.mark.gpu
 def test_threshold_rows_are_the_topm_lists_cut_at_tau():
-    w = W.WORKLOADS["embed_10m"].scaled(50000)
+    # 300,000 points: 1,172 blocks of counts, so the scan of block totals
+    # carries across two chunks of 1,024
+    w = W.WORKLOADS["embed_10m"].scaled(300_000)
     X = W.make_data(w).cuda()
     p = params_to_device(*W.make_init(w, X.cpu()))
     tau, m = 0.05, 8
