@@ -345,6 +345,7 @@ def run_ours(args, w, ws, rank, local):
                 "peak_gbs": float(peaks["hbm_gbs"])},
         "gpu_launches": launches,
         "clocks": clk.summary(),
+        "plan": G.gmm_plan_info(w.N, w.D, w.K, w.cov, w.x_dtype, precision=args.precision, plan=args.plan),
     }
     if e2e is not None:
         line["e2e"] = e2e

@@ -79,6 +79,8 @@ def lib():
         L.gmm_last_error.restype = ctypes.c_char_p
         L.gmm_release.argtypes = []
         L.gmm_release.restype = None
+        L.gmm_plan_info.argtypes = [i64, i32, i32, i32, i32, ctypes.POINTER(gmm_opts), ctypes.POINTER(ctypes.c_int32)]
+        L.gmm_plan_info.restype = ctypes.c_int
         L.gmm_last_launch_count.argtypes = []
         L.gmm_last_launch_count.restype = ctypes.c_int32
         L.gmm_profile_begin.argtypes = []
@@ -289,6 +291,19 @@ def gmm_reserve(N, D, K, cov="diag", x_dtype="bf16", **opt_kw):
     dt = BF16 if x_dtype in ("bf16", BF16) else F32
     o = gmm_default_opts(**opt_kw)
     _check(lib().gmm_reserve(int(N), int(D), int(K), cov_i, dt, ctypes.byref(o)))
+
+
+def gmm_plan_info(N, D, K, cov="diag", x_dtype="bf16", **opt_kw) -> dict:
+    """The launch plan of an EM step with these arguments on the current device
+    (see gmm_plan_info in include/gmm.h)."""
+    cov_i = COV[cov] if isinstance(cov, str) else int(cov)
+    dt = BF16 if x_dtype in ("bf16", BF16) else F32
+    o = gmm_default_opts(**opt_kw)
+    info = (ctypes.c_int32 * 8)()
+    _check(lib().gmm_plan_info(int(N), int(D), int(K), cov_i, dt, ctypes.byref(o), info))
+    keys = ("cluster", "tile_groups", "two_pass", "tile_groups_pass1", "flush_tiles", "threads",
+            "noalloc_tile_groups", "tiles")
+    return dict(zip(keys, [int(v) for v in info]))
 
 
 def gmm_stream_status(stream=None) -> int:

@@ -60,9 +60,11 @@ struct Plan {
   int tg1;            // tile groups of pass 1 (two-pass)
   int F;
   int flush;
-  size_t smem;
+  size_t smem;        // dynamic shared memory of the E-step kernel
+  bool emfast;        // FAST E-step passes run the two-team kernel (em_fast.cu)
+  int threads;        // threads per CTA of the E-step kernel
   // workspace offsets
-  size_t off_meta, off_pimg, off_cadj, off_iscale, off_part, off_llpart, off_lsepart, off_lse, off_ll;
+  size_t off_meta, off_pimg, off_cimg, off_cadj, off_iscale, off_part, off_llpart, off_lsepart, off_lse, off_ll;
   // tied covariance (cov_diag == 2): L, Sigma^-1, solve scratch, log|Sigma|, Gram
   // matrix and its partials, per-component (N_k, nu_k), covariance scratch
   size_t off_tl, off_sinv, off_twork, off_logdet, off_gram, off_gpart, off_tstats, off_tsig;
@@ -112,7 +114,7 @@ const void* fused_fn(int np, int nch, int nst, bool topm = false) {
 }
 
 // Largest number of C-CTA clusters of the fused kernel resident at once.
-int max_clusters(const void* fn, size_t smem, int C) {
+int max_clusters(const void* fn, size_t smem, int C, int threads) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, int> cache;
   std::lock_guard<std::mutex> lk(mu);
@@ -129,7 +131,7 @@ int max_clusters(const void* fn, size_t smem, int C) {
   if (C > 1) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C * n, 1, 1);
-    cfg.blockDim = dim3(416, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -178,21 +180,23 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   if (p.two_pass && !split) p.n_slices = (p.n_slices + 7) / 8 * 8;   // whole 8-slice groups for pass 1
   p.K_pad = p.n_slices * kSlice;
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
-  p.smem = fused_smem(p.np, p.nch, p.nst);
+  p.emfast = p.fast;
+  p.smem = p.emfast ? emfast_smem(p.nch) : fused_smem(p.np, p.nch, p.nst);
+  p.threads = p.emfast ? kEmFastThreads : 416;
   p.F = 2 * p.nch * kAtomElems + 1;
-  p.flush = p.fast ? 128 : 16;
+  p.flush = p.fast ? 256 : 16;
   const int sms = need_device ? device_sms() : 148;
-  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  const void* fn = p.emfast ? emfast_handle(p.nch, p.two_pass ? MODE_LSE : MODE_EM) : fused_fn(p.np, p.nch, p.nst);
   if (!p.two_pass) {
     p.C = p.n_slices;
     p.n_kgroups = 1;
-    int mc = need_device ? max_clusters(fn, p.smem, p.C) : std::max(1, sms / p.C);
+    int mc = need_device ? max_clusters(fn, p.smem, p.C, p.threads) : std::max(1, sms / p.C);
     p.tg = std::max(1, std::min(p.n_tiles, mc));
     p.tg1 = 0;
   } else {
     p.C = p.C1;
     p.n_kgroups = p.n_slices / p.C1;
-    int mc = p.C1 == 1 ? sms : (need_device ? max_clusters(fn, p.smem, p.C1) : std::max(1, sms / p.C1));
+    int mc = p.C1 == 1 ? sms : (need_device ? max_clusters(fn, p.smem, p.C1, p.threads) : std::max(1, sms / p.C1));
     p.tg1 = std::max(1, std::min(p.n_tiles, mc / p.n_kgroups));
     p.tg = std::max(1, std::min(p.n_tiles, sms / p.n_slices));
   }
@@ -202,6 +206,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.off_ll = off; off += 256;
   const size_t piece = static_cast<size_t>(2 * p.nch) * kChunkBytes;
   p.off_pimg = off; off += align256(static_cast<size_t>(p.n_slices) * p.np * piece);
+  p.off_cimg = off; off += align256(static_cast<size_t>(p.n_slices) * kConstBytes);
   p.off_cadj = off; off += align256(sizeof(float) * p.K_pad);
   p.off_iscale = off; off += align256(sizeof(float) * p.K_pad);
   p.off_part = off; off += align256(sizeof(double) * static_cast<size_t>(p.tg) * p.K_pad * p.F);
@@ -439,10 +444,16 @@ int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, con
       if (r) return r;
     }
   }
+  if (p.fast) {
+    // the one parameter scale of FAST needs the largest coefficient first
+    int r = launch(kernel_handle(K_BMAX), dim3(p.K), dim3(128), 0, s, 1, mu, var, p.D, p.K, p.cov_diag, meta,
+                   static_cast<const double*>(sinv));
+    if (r) return r;
+  }
   {
     const void* fn = kernel_handle(p.fast ? K_PARAMS_FAST : K_PARAMS_PRECISE);
-    int r = launch(fn, dim3(p.K_pad), dim3(128), 0, s, 1, lw, mu, var, p.D, p.K, p.cov_diag, p.nch,
-                   static_cast<const Meta*>(meta), ws + p.off_pimg, reinterpret_cast<float*>(ws + p.off_cadj),
+    int r = launch(fn, dim3(p.K_pad), dim3(128), 0, s, 1, lw, mu, var, p.D, p.K, p.cov_diag, p.nch, meta,
+                   ws + p.off_pimg, ws + p.off_cimg, reinterpret_cast<float*>(ws + p.off_cadj),
                    reinterpret_cast<float*>(ws + p.off_iscale), status, static_cast<const double*>(sinv),
                    static_cast<const double*>(logdet));
     if (r) return r;
@@ -475,6 +486,7 @@ FusedArgs base_args(const Plan& p, const void* X, uint8_t* ws) {
   a.flush_tiles = p.flush;
   a.F = p.F;
   a.p_img = ws + p.off_pimg;
+  a.c_img = ws + p.off_cimg;
   a.cadj = reinterpret_cast<const float*>(ws + p.off_cadj);
   a.iscale = reinterpret_cast<const float*>(ws + p.off_iscale);
   a.meta = reinterpret_cast<const Meta*>(ws + p.off_meta);
@@ -490,22 +502,34 @@ FusedArgs base_args(const Plan& p, const void* X, uint8_t* ws) {
 // normaliser pass + combine + statistics pass.  The statistics add into the
 // partials at a.part (zeroed by the caller once per EM step); the
 // log-likelihood partials go to ll_part, *n_ll of them.
+// The E-step kernel of a plan (the two-team kernel for FAST).
+const void* estep_fn(const Plan& p, int mode) {
+  return p.emfast ? emfast_handle(p.nch, mode) : fused_fn(p.np, p.nch, p.nst);
+}
+
+// Raise the shared-memory limit of every E-step kernel the plan launches.
+int set_estep_attrs(const Plan& p) {
+  int r;
+  if (!p.two_pass) return set_smem_attr(estep_fn(p, MODE_EM), p.smem);
+  if ((r = set_smem_attr(estep_fn(p, MODE_LSE), p.smem))) return r;
+  return set_smem_attr(estep_fn(p, MODE_GIVEN), p.smem);
+}
+
 int run_estep(const Plan& p, const FusedArgs& a, uint8_t* ws, double* ll_part, cudaStream_t s, int* n_ll) {
-  const void* fn = fused_fn(p.np, p.nch, p.nst);
   int r;
   if (!p.two_pass) {
     FusedArgs a0 = a;
     a0.mode = MODE_EM;
     a0.C = p.C;
     a0.ll_part = ll_part;
-    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), p.smem, s, p.C, a0))) return r;
+    if ((r = launch_main(estep_fn(p, MODE_EM), dim3(p.C * p.tg, 1), dim3(p.threads), p.smem, s, p.C, a0))) return r;
     *n_ll = p.tg * p.C;   // one log-likelihood partial per CTA
   } else {
     // pass 1: per-point normaliser over each group of 1024 components
     FusedArgs a1 = a;
     a1.mode = MODE_LSE;
     a1.C = p.C1;
-    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), p.smem, s, p.C1, a1))) return r;
+    if ((r = launch_main(estep_fn(p, MODE_LSE), dim3(p.C1 * p.tg1, p.n_kgroups), dim3(p.threads), p.smem, s, p.C1, a1))) return r;
     float* lse = reinterpret_cast<float*>(ws + p.off_lse);
     if ((r = launch(kernel_handle(K_LSE_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
                     static_cast<const float*>(a.lse_part), p.n_kgroups, p.N, lse, ll_part)))
@@ -516,7 +540,7 @@ int run_estep(const Plan& p, const FusedArgs& a, uint8_t* ws, double* ll_part, c
     a2.mode = MODE_GIVEN;
     a2.C = 1;
     a2.ll_part = nullptr;
-    if ((r = launch_main(fn, dim3(p.n_slices, p.tg), dim3(416), p.smem, s, 1, a2))) return r;
+    if ((r = launch_main(estep_fn(p, MODE_GIVEN), dim3(p.n_slices, p.tg), dim3(p.threads), p.smem, s, 1, a2))) return r;
   }
   return GMM_OK;
 }
@@ -613,6 +637,7 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
              const TopmSpace& ts, cudaStream_t s) {
   const int maxm = m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
   const void* fn = fused_fn(p.np, p.nch, p.nst, true);
+  const size_t smem = fused_smem(p.np, p.nch, p.nst);
   FusedArgs a = base_args(p, X, ws);
   a.mode = MODE_TOPM;
   a.topm = m;
@@ -624,7 +649,7 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
     a.topm_groups = 1;
     a.topm_val = resp_out;
     a.topm_idx = idx_out;
-    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), p.smem, s, p.C, a))) return r;
+    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), smem, s, p.C, a))) return r;
     if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
                               static_cast<const double*>(a.ll_part), p.tg * p.C, ll_dev)))
       return r;
@@ -633,7 +658,7 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
     a.topm_groups = p.n_kgroups;
     a.topm_val = reinterpret_cast<float*>(ws + ts.off_gval);
     a.topm_idx = reinterpret_cast<int32_t*>(ws + ts.off_gidx);
-    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), p.smem, s, p.C1, a))) return r;
+    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), smem, s, p.C1, a))) return r;
     if ((r = launch(kernel_handle(K_TOPM_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
                     static_cast<const float*>(a.lse_part), static_cast<const float*>(a.topm_val),
                     static_cast<const int32_t*>(a.topm_idx), p.n_kgroups, p.N, m, resp_out, idx_out,
@@ -714,8 +739,7 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = nullptr;
   if ((r = get_workspace(p.ws_bytes, &ws))) return r;
-  const void* fn = fused_fn(p.np, p.nch, p.nst);
-  if ((r = set_smem_attr(fn, p.smem))) return r;
+  if ((r = set_estep_attrs(p))) return r;
 
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
   CUDA_TRY(cudaMemsetAsync(ws + p.off_part, 0, sizeof(double) * static_cast<size_t>(p.tg) * p.K_pad * p.F, s));
@@ -765,8 +789,7 @@ int gmm_em_step_host(const void* X_host, int64_t N, int32_t D, int32_t K, int32_
   if ((r = get_workspace(off_stage + 2 * stage_bytes, &ws))) return r;
   HostPipe* hp = nullptr;
   if ((r = get_pipe(&hp))) return r;
-  const void* fn = fused_fn(p.np, p.nch, p.nst);
-  if ((r = set_smem_attr(fn, p.smem))) return r;
+  if ((r = set_estep_attrs(p))) return r;
 
   // the copies may overwrite the staging buffers only once the work already
   // on the stream (an earlier call's kernels) is done
@@ -821,7 +844,7 @@ int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = nullptr;
   if ((r = get_workspace(ts.end, &ws))) return r;
-  if ((r = set_smem_attr(fused_fn(p.np, p.nch, p.nst, true), p.smem))) return r;
+  if ((r = set_smem_attr(fused_fn(p.np, p.nch, p.nst, true), fused_smem(p.np, p.nch, p.nst)))) return r;
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
   double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
   if ((r = run_topm(p, X, m, resp_out, idx_out, ll_dev, ws, ts, s))) return r;
@@ -864,7 +887,7 @@ int gmm_assign_threshold(const void* X, int64_t N, int32_t D, int32_t K, int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = nullptr;
   if ((r = get_workspace(ts.end, &ws))) return r;
-  if ((r = set_smem_attr(fused_fn(p.np, p.nch, p.nst, true), p.smem))) return r;
+  if ((r = set_smem_attr(fused_fn(p.np, p.nch, p.nst, true), fused_smem(p.np, p.nch, p.nst)))) return r;
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
   float* tr = reinterpret_cast<float*>(ws + off_r);
   int32_t* ti = reinterpret_cast<int32_t*>(ws + off_i);
@@ -1008,6 +1031,34 @@ int noalloc_scratch(uint8_t** out) {
   *out = g_noalloc_base[dev];
   return GMM_OK;
 }
+
+// Scratch layout of gmm_em_step_noalloc inside the fixed array; the number of
+// tile groups (and so of CTAs) is lowered until the per-group statistics fit.
+int noalloc_layout(Plan& p) {
+  const size_t piece = static_cast<size_t>(2 * p.nch) * kChunkBytes;
+  const size_t row_bytes = sizeof(double) * static_cast<size_t>(p.K_pad) * p.F;
+  size_t fixed = kStatusBytes + align256(sizeof(Meta)) + 256 +
+                 align256(static_cast<size_t>(p.n_slices) * p.np * piece) +
+                 align256(static_cast<size_t>(p.n_slices) * kConstBytes) + 2 * align256(sizeof(float) * p.K_pad) +
+                 align256(sizeof(double) * kCombineBlocks);
+  if (fixed + align256(row_bytes) > kNoAllocScratchBytes)
+    return fail(GMM_ERR_UNSUPPORTED, "problem too large for the 40 MiB scratch of gmm_em_step_noalloc");
+  const int tg_fit = static_cast<int>((kNoAllocScratchBytes - fixed) / row_bytes);
+  p.tg = std::max(1, std::min(p.tg, tg_fit));
+  size_t off = kStatusBytes;
+  p.off_meta = off; off += align256(sizeof(Meta));
+  p.off_ll = off; off += 256;
+  p.off_pimg = off; off += align256(static_cast<size_t>(p.n_slices) * p.np * piece);
+  p.off_cimg = off; off += align256(static_cast<size_t>(p.n_slices) * kConstBytes);
+  p.off_cadj = off; off += align256(sizeof(float) * p.K_pad);
+  p.off_iscale = off; off += align256(sizeof(float) * p.K_pad);
+  p.off_llpart = off; off += align256(sizeof(double) * std::max<size_t>(static_cast<size_t>(p.tg) * p.C, kCombineBlocks));
+  p.off_part = off; off += align256(row_bytes * p.tg);
+  p.off_lsepart = p.off_lse = off;
+  if (off > kNoAllocScratchBytes) return fail(GMM_ERR_UNSUPPORTED, "scratch layout overflow");
+
+  return GMM_OK;
+}
 }  // namespace
 
 extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type,
@@ -1033,42 +1084,22 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
   if (p.two_pass)
     return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_noalloc supports K <= 1024 (larger K needs an N-sized buffer)");
 
-  // Scratch layout inside the fixed array; the number of tile groups (and so
-  // of CTAs) is lowered until the per-group statistics fit.
-  const size_t piece = static_cast<size_t>(2 * p.nch) * kChunkBytes;
-  const size_t row_bytes = sizeof(double) * static_cast<size_t>(p.K_pad) * p.F;
-  size_t fixed = kStatusBytes + align256(sizeof(Meta)) + 256 +
-                 align256(static_cast<size_t>(p.n_slices) * p.np * piece) + 2 * align256(sizeof(float) * p.K_pad) +
-                 align256(sizeof(double) * kCombineBlocks);
-  if (fixed + align256(row_bytes) > kNoAllocScratchBytes)
-    return fail(GMM_ERR_UNSUPPORTED, "problem too large for the 40 MiB scratch of gmm_em_step_noalloc");
-  const int tg_fit = static_cast<int>((kNoAllocScratchBytes - fixed) / row_bytes);
-  p.tg = std::max(1, std::min(p.tg, tg_fit));
-  size_t off = kStatusBytes;
-  p.off_meta = off; off += align256(sizeof(Meta));
-  p.off_ll = off; off += 256;
-  p.off_pimg = off; off += align256(static_cast<size_t>(p.n_slices) * p.np * piece);
-  p.off_cadj = off; off += align256(sizeof(float) * p.K_pad);
-  p.off_iscale = off; off += align256(sizeof(float) * p.K_pad);
-  p.off_llpart = off; off += align256(sizeof(double) * std::max<size_t>(static_cast<size_t>(p.tg) * p.C, kCombineBlocks));
-  p.off_part = off; off += align256(row_bytes * p.tg);
-  p.off_lsepart = p.off_lse = off;
-  if (off > kNoAllocScratchBytes) return fail(GMM_ERR_UNSUPPORTED, "scratch layout overflow");
-
+  if ((r = noalloc_layout(p))) return r;
   uint8_t* ws = nullptr;
   if ((r = noalloc_scratch(&ws))) return r;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const void* fn = fused_fn(p.np, p.nch, p.nst);
+  const void* fn = estep_fn(p, MODE_EM);
   if ((r = set_smem_attr(fn, p.smem))) return r;
   // the array keeps the previous call's contents: clear the status words and
   // the statistics accumulators, which must start at zero
   CUDA_TRY(cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), s));
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
+  const size_t row_bytes = sizeof(double) * static_cast<size_t>(p.K_pad) * p.F;
   CUDA_TRY(cudaMemsetAsync(ws + p.off_part, 0, row_bytes * p.tg, s));
   FusedArgs a = base_args(p, X, ws);
   a.mode = MODE_EM;
   a.C = p.C;
-  if ((r = launch(fn, dim3(p.C * p.tg, 1), dim3(416), p.smem, s, p.C, a))) return r;
+  if ((r = launch(fn, dim3(p.C * p.tg, 1), dim3(p.threads), p.smem, s, p.C, a))) return r;
   double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
   {
     float reg = o.reg_covar, floor_ = o.var_floor;
@@ -1086,6 +1117,34 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
     uint32_t st[2] = {0, 0};
     CUDA_TRY(cudaMemcpy(st, ws, sizeof(st), cudaMemcpyDeviceToHost));
     if (st[0]) return status_to_code(st[0], st[1]);
+  }
+  return GMM_OK;
+}
+
+extern "C" int gmm_plan_info(int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
+                             const gmm_opts* opts, int32_t* info) {
+  if (!info) return fail(GMM_ERR_INVALID_ARG, "info is NULL");
+  gmm_opts o;
+  gmm_default_opts(&o);
+  if (opts) o = *opts;
+  Plan p;
+  int r;
+  if ((r = make_plan(p, nullptr, N, D, K, cov_type, x_dtype, o, true))) return r;
+  info[0] = p.two_pass ? p.C1 : p.C;
+  info[1] = p.tg;
+  info[2] = p.two_pass ? 1 : 0;
+  info[3] = p.two_pass ? p.tg1 : 0;
+  info[4] = p.flush;
+  info[5] = p.threads;
+  info[6] = 0;
+  info[7] = p.n_tiles;
+  if (cov_type != GMM_TIED) {
+    gmm_opts on = o;
+    on.plan = GMM_PLAN_CLUSTER;
+    Plan pn;
+    if (make_plan(pn, nullptr, N, D, K, cov_type, x_dtype, on, true) == GMM_OK && !pn.two_pass &&
+        noalloc_layout(pn) == GMM_OK)
+      info[6] = pn.tg;
   }
   return GMM_OK;
 }

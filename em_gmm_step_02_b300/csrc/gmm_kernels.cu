@@ -30,50 +30,11 @@
 #include "gmm_kernels.cuh"
 #include "layout.cuh"
 #include "ptx.cuh"
+#include "common.cuh"
+#include "transform.cuh"
 
 namespace gmm {
 
-constexpr double kLog2e = 1.4426950408889634073599246810019;
-constexpr double kLn2 = 0.69314718055994530941723212145818;
-constexpr double kLog2Pi = 1.8378770664093454835606594728112;  // ln(2 pi)
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float lg2(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool cond) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r) : "r"(static_cast<uint32_t>(cond)), "r"(id), "r"(nthreads) : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ void red_add_f64(double* p, double v) {
-  asm volatile("red.global.add.f64 [%0], %1;" :: "l"(p), "d"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t sq_f16x2(uint32_t x) {
-  __half2 h = *reinterpret_cast<__half2*>(&x);
-  h = __hmul2(h, h);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 // ============================================================== scan of |X|
 __global__ void absmax_kernel(const void* __restrict__ X, int64_t n_elems, int x_bf16,
@@ -158,7 +119,44 @@ __global__ void meta_kernel(const float* __restrict__ means, int D, int K, int u
     }
     meta->scale = scale;
     meta->inv_scale = 1.f / scale;
+    meta->bmax_bits = 0u;
   }
+}
+
+// ============================================================== bmax (FAST)
+// Largest magnitude over all components and features of the logit
+// coefficients mu'/s2' and 1/(2 s2') (log2 units; tied: (Sigma^-1 nu)_d /
+// scale): FAST gives every parameter row the same power-of-two scale, so the
+// accumulated logits need one multiplier only.  One block per component.
+__global__ void bmax_kernel(const float* __restrict__ means, const float* __restrict__ vars, int D, int K,
+                            int cov_diag, Meta* __restrict__ meta, const double* __restrict__ sinv) {
+  const int k = blockIdx.x;
+  const int d = threadIdx.x;   // blockDim.x == 128
+  __shared__ double nu[kMaxD];
+  __shared__ float red[128];
+  float m = 0.f;
+  if (cov_diag == 2) {
+    if (k < K && d < D) nu[d] = static_cast<double>(means[static_cast<int64_t>(k) * D + d]) - meta->shift[d];
+    __syncthreads();
+    if (k < K && d < D) {
+      double w = 0.0;
+      for (int e = 0; e < D; ++e) w += sinv[static_cast<int64_t>(d) * D + e] * nu[e];
+      m = static_cast<float>(fabs(w / meta->scale * kLog2e));
+    }
+  } else if (k < K && d < D) {
+    const double sc = meta->scale;
+    const double mup = (static_cast<double>(means[static_cast<int64_t>(k) * D + d]) - meta->shift[d]) * sc;
+    const double vp = static_cast<double>(cov_diag ? vars[static_cast<int64_t>(k) * D + d] : vars[k]) * sc * sc;
+    if (vp > 0.0) m = static_cast<float>(fmax(fabs(mup / vp), 0.5 / vp) * kLog2e);
+  }
+  if (!(m < 3e38f)) m = 0.f;   // non-finite parameters are reported by params_kernel
+  red[d] = m;
+  __syncthreads();
+  for (int o = 64; o > 0; o >>= 1) {
+    if (d < o) red[d] = fmaxf(red[d], red[d + o]);
+    __syncthreads();
+  }
+  if (d == 0) atomicMax(&meta->bmax_bits, __float_as_uint(red[0]));
 }
 
 // ============================================================== params
@@ -169,6 +167,16 @@ __global__ void meta_kernel(const float* __restrict__ means, int D, int K, int u
 //   columns [Dp, Dp + D)  -1/(2 s2') * log2(e)     (x^2-part)
 // in the same swizzled K-major layout as the data tiles, and the logit
 // constant in log2 units.  x' = (x - shift) * scale, s2' = s2 * scale^2.
+//
+// FAST: every row carries the same power-of-two scale (from bmax_kernel), and
+// the constant is the one of the Gaussian that the fp16-rounded row describes
+// exactly: with b1, b2 the rounded coefficients, that Gaussian has
+// s2' = -log2(e) / (2 b2) and mu' = -b1 / (2 b2), so the logit is a properly
+// normalised log-density and the rounding only moves mu and s2 by relative
+// amounts of 2^-12 (instead of adding an offset to every logit of the row).
+// The constant also goes, split into three fp16 pieces, into the 128 x 16
+// constant operand of the slice (c_img), which turns it into one more K step
+// of the logit contraction.
 //
 // Tied covariance (cov == 2; Sigma shared, its inverse `sinv` and log|Sigma|
 // from tied_prep_kernel): the logit drops its per-point term
@@ -181,7 +189,7 @@ __global__ void meta_kernel(const float* __restrict__ means, int D, int K, int u
 template <bool kFast>
 __global__ void params_kernel(const float* __restrict__ log_weights, const float* __restrict__ means,
                               const float* __restrict__ vars, int D, int K, int cov_diag, int nch,
-                              const Meta* __restrict__ meta, uint8_t* __restrict__ p_img,
+                              Meta* __restrict__ meta, uint8_t* __restrict__ p_img, uint8_t* __restrict__ c_img,
                               float* __restrict__ cadj, float* __restrict__ iscale,
                               uint32_t* __restrict__ status, const double* __restrict__ sinv,
                               const double* __restrict__ tied_logdet) {
@@ -194,6 +202,8 @@ __global__ void params_kernel(const float* __restrict__ log_weights, const float
   double b1 = 0.0, b2 = 0.0, cpart = 0.0;
   bool bad = false;
   __shared__ double nu[kMaxD];
+  const double sc = meta->scale;
+  double v_nat = 1.0, mup = 0.0, vp = 1.0;
   if (cov_diag == 2) {
     // tied: nu = mu_k - shift, then b1 = Sigma^-1 nu / scale
     if (valid_k && d < D) {
@@ -205,21 +215,44 @@ __global__ void params_kernel(const float* __restrict__ log_weights, const float
     if (valid_k && d < D) {
       double w = 0.0;
       for (int e = 0; e < D; ++e) w += sinv[static_cast<int64_t>(d) * D + e] * nu[e];
-      b1 = w / meta->scale * kLog2e;
+      b1 = w / sc * kLog2e;
       cpart = nu[d] * w;
     }
   } else if (valid_k && d < D) {
     const float mu = means[static_cast<int64_t>(k) * D + d];
     const float v = cov_diag ? vars[static_cast<int64_t>(k) * D + d] : vars[k];
     bad = !isfinite(mu) || !isfinite(v) || !(v > 0.f);
-    const double sc = meta->scale;
-    const double mup = (static_cast<double>(mu) - meta->shift[d]) * sc;
-    const double vp = static_cast<double>(v) * sc * sc;
+    mup = (static_cast<double>(mu) - meta->shift[d]) * sc;
+    vp = static_cast<double>(v) * sc * sc;
+    v_nat = v;
     b1 = mup / vp * kLog2e;
     b2 = -0.5 / vp * kLog2e;
     cpart = log(static_cast<double>(v)) + kLog2Pi + mup * mup / vp;
   }
   if (bad) atomicOr(status, ST_NONFINITE);
+  // scale of the fp16 rows: FAST one for all components, PRECISE per component
+  float s = 1.f;
+  if (kFast) {
+    const float bm = __uint_as_float(meta->bmax_bits);
+    if (bm > 0.f) s = ldexpf(1.f, max(-120, min(120, static_cast<int>(floorf(log2f(16384.f / bm))))));
+    if (k == 0 && d == 0) {
+      meta->pscale = s;
+      meta->pinv = 1.f / s;
+    }
+  }
+  // FAST diagonal / spherical: the constant of the Gaussian the rounded row
+  // describes, summed in log2 units (see above); otherwise the exact one
+  const bool consistent = kFast && cov_diag != 2;
+  if (consistent && valid_k && d < D) {
+    const double h1 = __half2float(__float2half_rn(static_cast<float>(b1 * s))) / s;
+    const double h2 = __half2float(__float2half_rn(static_cast<float>(b2 * s))) / s;
+    if (h2 < 0.0) {
+      const double vpe = -0.5 * kLog2e / h2;
+      cpart = 0.5 * kLog2e * (kLog2Pi + log(vpe) - 2.0 * log(sc)) - h1 * h1 / (4.0 * h2);
+    } else {
+      cpart = 0.5 * kLog2e * (log(v_nat) + kLog2Pi + mup * mup / vp);
+    }
+  }
   red_c[d] = cpart;
   red_m[d] = static_cast<float>(fmax(fabs(b1), fabs(b2)));
   __syncthreads();
@@ -230,25 +263,50 @@ __global__ void params_kernel(const float* __restrict__ log_weights, const float
     }
     __syncthreads();
   }
-  // per-component scale keeping the fp16 operands in range
-  float s = 1.f;
-  if (red_m[0] > 0.f) {
+  if (!kFast && red_m[0] > 0.f) {
     int e = static_cast<int>(floorf(log2f(16384.f / red_m[0])));
     s = ldexpf(1.f, max(-120, min(120, e)));
   }
-  if (d == 0) {
-    float lw = valid_k ? log_weights[k] : -CUDART_INF_F;
-    if (valid_k && (lw != lw || lw == CUDART_INF_F)) atomicOr(status, ST_NONFINITE);
-    float c = -CUDART_INF_F;
+  const int slice = k / kSlice, row = k % kSlice;
+  double cval = -CUDART_INF;   // logit constant, log2 units
+  {
+    const float lw = valid_k ? log_weights[k] : -CUDART_INF_F;
+    if (d == 0 && valid_k && (lw != lw || lw == CUDART_INF_F)) atomicOr(status, ST_NONFINITE);
     if (valid_k && lw > -CUDART_INF_F) {
-      const double q = cov_diag == 2 ? static_cast<double>(D) * kLog2Pi + *tied_logdet + red_c[0] : red_c[0];
-      c = static_cast<float>((static_cast<double>(lw) - 0.5 * q) * kLog2e);
+      if (consistent) {
+        cval = static_cast<double>(lw) * kLog2e - red_c[0];
+      } else {
+        const double q = cov_diag == 2 ? static_cast<double>(D) * kLog2Pi + *tied_logdet + red_c[0] : red_c[0];
+        cval = (static_cast<double>(lw) - 0.5 * q) * kLog2e;
+      }
     }
-    cadj[k] = c;
+  }
+  if (d == 0) {
+    cadj[k] = static_cast<float>(cval);
     iscale[k] = valid_k ? 1.f / s : 0.f;
   }
+  if (kFast && d < 16) {
+    // row `row` of the slice's constant operand: s * c in three fp16 pieces
+    __half piece = __float2half_rn(0.f);
+    if (d < 3) {
+      if (cval == -CUDART_INF) {
+        piece = d == 0 ? __float2half_rn(-CUDART_INF_F) : __float2half_rn(0.f);
+      } else {
+        double rem = cval * s;
+        if (!(fabs(rem) < 65504.0 * 32768.0)) {
+          atomicOr(status, ST_RANGE);
+          rem = 0.0;
+        }
+        for (int i = 0; i <= d; ++i) {
+          const __half h = __float2half_rn(static_cast<float>(ldexp(rem, -const_exp(i))));
+          if (i == d) piece = h;
+          rem -= ldexp(static_cast<double>(__half2float(h)), const_exp(i));
+        }
+      }
+    }
+    *reinterpret_cast<__half*>(c_img + static_cast<size_t>(slice) * kConstBytes + const_off(row, d)) = piece;
+  }
   // write this component's row of the operand images (thread d owns column d)
-  const int slice = k / kSlice, row = k % kSlice;
   const int np = kFast ? 1 : 2;
   const size_t piece_bytes = static_cast<size_t>(2 * nch) * kChunkBytes;
   uint8_t* img = p_img + static_cast<size_t>(slice) * np * piece_bytes;
@@ -397,162 +455,6 @@ __device__ __forceinline__ void topm_tile(const FusedArgs& a, Small* S, uint8_t*
   if (C > 1 && st == 0) {
     const uint32_t bar = smem_u32(&S->tfree);
     for (int r = 0; r < C; ++r) mbar_arrive_remote(mapa(bar, r));
-  }
-}
-
-// ============================================================== data transform
-// 16-byte load that bypasses L1 (each data tile is read once per SM).
-__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-// The four transform warps turn each 128-point tile of X into the two fp16
-// operand pieces [x' | x'^2] (PRECISE: hi and lo parts of each), with
-// x' = (x - shift) * scale, in the swizzled K-major layout of the data stage.
-// Thread `tid` owns one 8-feature unit of every RPP-th row.  All loads of a
-// tile are issued together (and, when the registers allow, one tile ahead)
-// so that the whole tile is in flight at once.
-template <typename CF, int NP, int NCH, int NST, bool XB, bool kTopm>
-__device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm, Small* S,
-                                                volatile uint32_t* abort_flag, int tid, int tgroup,
-                                                int n_tgroups, int my_tiles) {
-  constexpr int UPR = 8 * NCH;               // 8-feature units per row
-  constexpr int RPP = 128 / UPR;             // rows per pass of the 128 threads
-  constexpr int NPASS = 128 / RPP;
-  constexpr int W = XB ? 4 : 8;              // 32-bit words per unit
-  constexpr int NBATCH = (XB || NCH == 1) ? 1 : 2;
-  constexpr int NB = NPASS / NBATCH;
-  const int ch = tid % UPR;
-  const int r0 = tid / UPR;
-  const int d0 = ch * 8;
-  const Meta* meta = a.meta;
-  const float scale = meta->scale;
-  float nshift[8];                           // -shift * scale
-#pragma unroll
-  for (int e = 0; e < 8; ++e) nshift[e] = d0 + e < a.D ? -meta->shift[d0 + e] * scale : 0.f;
-  const bool vec = (a.D % 8) == 0;
-  const bool unit_in = d0 < a.D;
-  uint32_t buf[NB][W];
-
-  auto load_batch = [&](int t, int b) {
-#pragma unroll
-    for (int p = 0; p < NB; ++p) {
-      const int row = r0 + RPP * (b * NB + p);
-      const int64_t n = static_cast<int64_t>(t) * kBN + row;
-#pragma unroll
-      for (int e = 0; e < W; ++e) buf[p][e] = 0u;
-      if (n < a.N && unit_in) {
-        if constexpr (XB) {
-          const uint16_t* xr = static_cast<const uint16_t*>(a.X) + n * a.D + d0;
-          if (vec) {
-            const uint4 v = ldg_stream_v4(xr);
-            buf[p][0] = v.x; buf[p][1] = v.y; buf[p][2] = v.z; buf[p][3] = v.w;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (d0 + e < a.D) buf[p][e >> 1] |= static_cast<uint32_t>(__ldg(xr + e)) << (16 * (e & 1));
-          }
-        } else {
-          const float* xr = static_cast<const float*>(a.X) + n * a.D + d0;
-          if (vec) {
-            const uint4 v0 = ldg_stream_v4(xr);
-            const uint4 v1 = ldg_stream_v4(xr + 4);
-            buf[p][0] = v0.x; buf[p][1] = v0.y; buf[p][2] = v0.z; buf[p][3] = v0.w;
-            buf[p][4] = v1.x; buf[p][5] = v1.y; buf[p][6] = v1.z; buf[p][7] = v1.w;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (d0 + e < a.D) buf[p][e] = __float_as_uint(__ldg(xr + e));
-          }
-        }
-      }
-    }
-  };
-
-  auto store_batch = [&](int t, int b, uint8_t* stage, int s, int use) {
-#pragma unroll
-    for (int p = 0; p < NB; ++p) {
-      const int i = b * NB + p;
-      const int row = r0 + RPP * i;
-      // rows 16g..16g+15 of the stage are free once the statistics MMA of the
-      // stage's previous tile has consumed them
-      if ((RPP * i) % 16 == 0 && use > 0)
-        mbar_wait(&S->empty_g[s][(RPP * i) / 16], (use - 1) & 1, abort_flag, a.status);
-      const bool valid = static_cast<int64_t>(t) * kBN + row < a.N;
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float v;
-        if constexpr (XB) v = __uint_as_float((e & 1) ? (buf[p][e >> 1] & 0xffff0000u) : (buf[p][e >> 1] << 16));
-        else v = __uint_as_float(buf[p][e]);
-        // bf16 data in FAST are never shifted, and rows beyond N were loaded as
-        // zeros, so the plain scaling already leaves those rows zero
-        if constexpr (XB && NP == 1) x[e] = v * scale;
-        else x[e] = valid ? fmaf(v, scale, nshift[e]) : 0.f;
-      }
-      const uint32_t off = (ch / 8) * kChunkBytes + sw128_off(row, ch % 8);
-      const uint32_t off2 = off + NCH * kChunkBytes;
-      if constexpr (NP == 1) {
-        uint4 hx, hq;
-        hx.x = pack_f16x2(x[0], x[1]); hx.y = pack_f16x2(x[2], x[3]);
-        hx.z = pack_f16x2(x[4], x[5]); hx.w = pack_f16x2(x[6], x[7]);
-        if (XB) {
-          // bf16 data scaled by a power of two are exact in fp16, so the
-          // fp16 square of the packed value rounds the exact x'^2 once
-          hq.x = sq_f16x2(hx.x); hq.y = sq_f16x2(hx.y); hq.z = sq_f16x2(hx.z); hq.w = sq_f16x2(hx.w);
-        } else {
-          hq.x = pack_f16x2(x[0] * x[0], x[1] * x[1]); hq.y = pack_f16x2(x[2] * x[2], x[3] * x[3]);
-          hq.z = pack_f16x2(x[4] * x[4], x[5] * x[5]); hq.w = pack_f16x2(x[6] * x[6], x[7] * x[7]);
-        }
-        *reinterpret_cast<uint4*>(stage + off) = hx;
-        *reinterpret_cast<uint4*>(stage + off2) = hq;
-      } else {
-        float xh[8], xl[8], qh[8], ql[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          xh[e] = __half2float(__float2half_rn(x[e]));
-          xl[e] = x[e] - xh[e];
-          const float q = x[e] * x[e];
-          qh[e] = __half2float(__float2half_rn(q));
-          ql[e] = q - qh[e];
-        }
-        uint4 v;
-        v.x = pack_f16x2(xh[0], xh[1]); v.y = pack_f16x2(xh[2], xh[3]);
-        v.z = pack_f16x2(xh[4], xh[5]); v.w = pack_f16x2(xh[6], xh[7]);
-        *reinterpret_cast<uint4*>(stage + off) = v;
-        v.x = pack_f16x2(qh[0], qh[1]); v.y = pack_f16x2(qh[2], qh[3]);
-        v.z = pack_f16x2(qh[4], qh[5]); v.w = pack_f16x2(qh[6], qh[7]);
-        *reinterpret_cast<uint4*>(stage + off2) = v;
-        v.x = pack_f16x2(xl[0], xl[1]); v.y = pack_f16x2(xl[2], xl[3]);
-        v.z = pack_f16x2(xl[4], xl[5]); v.w = pack_f16x2(xl[6], xl[7]);
-        *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off) = v;
-        v.x = pack_f16x2(ql[0], ql[1]); v.y = pack_f16x2(ql[2], ql[3]);
-        v.z = pack_f16x2(ql[4], ql[5]); v.w = pack_f16x2(ql[6], ql[7]);
-        *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off2) = v;
-      }
-    }
-  };
-
-  const int nst = kTopm ? 1 : NST;
-  if (NBATCH == 1 && my_tiles > 0) load_batch(tgroup, 0);
-  int t = tgroup;
-#pragma unroll 1
-  for (int j = 0; j < my_tiles; ++j, t += n_tgroups) {
-    // (no early exit on an abort: every wait below returns at once after one,
-    // so the loop runs out quickly and every barrier still sees all its threads)
-    const int s = j % nst, use = j / nst;
-    uint8_t* stage = sm + CF::kOffA + s * CF::kStageBytes;
-#pragma unroll
-    for (int b = 0; b < NBATCH; ++b) {
-      if (NBATCH > 1) load_batch(t, b);
-      store_batch(t, b, stage, s, use);
-    }
-    fence_proxy_async_smem();
-    mbar_arrive(&S->full_a[s]);
-    if (NBATCH == 1 && j + 1 < my_tiles) load_batch(t + n_tgroups, 0);
   }
 }
 
@@ -822,7 +724,9 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
   }
   const int kbase = slice * kSlice;
   const int kvalid = max(0, min(kSlice, a.K - kbase));
-  const int n1 = max(16, min(kSlice, (kvalid + 15) & ~15));         // logit MMA width
+  // every logit column is computed: padded components have zero operand rows
+  // and a -inf constant, so their logits are -inf whatever tensor memory held
+  const int n1 = kSlice;
   int my_tiles = 0;
   if (tgroup < a.n_tiles) my_tiles = (a.n_tiles - 1 - tgroup) / n_tgroups + 1;
 
@@ -888,8 +792,8 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
   if (warp < 4) {
     // ================================================= transform warps
     if constexpr (kRegSplit) regs_release<112>();
-    if (a.x_bf16) transform_warps<CF, NP, NCH, NST, true, kTopm>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
-    else transform_warps<CF, NP, NCH, NST, false, kTopm>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
+    if (a.x_bf16) transform_warps<CF, Small, NP, NCH, NST, true, kTopm>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
+    else transform_warps<CF, Small, NP, NCH, NST, false, kTopm>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
   } else if (warp < 12 && NP == 1 && !kTopm) {
     // ================================================= softmax warps (FAST EM)
     if constexpr (kRegSplit) regs_claim<136>();
@@ -1709,6 +1613,7 @@ const void* kernel_handle(KernelId id) {
     case K_GRAM_REDUCE: return reinterpret_cast<const void*>(&gram_reduce_kernel);
     case K_GRAM_REDUCE_F32: return reinterpret_cast<const void*>(&gram_reduce_f32_kernel);
     case K_SIGMA_TIED: return reinterpret_cast<const void*>(&sigma_tied_kernel);
+    case K_BMAX: return reinterpret_cast<const void*>(&bmax_kernel);
   }
   return nullptr;
 }

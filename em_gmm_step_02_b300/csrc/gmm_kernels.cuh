@@ -29,6 +29,9 @@ struct Meta {
   float scale;            // power of two
   float inv_scale;
   uint32_t absmax_bits;   // max |x| over X (float bits; written by the scan)
+  uint32_t bmax_bits;     // FAST: max over components and features of |mu'/s2'|, |1/(2 s2')| (log2 units)
+  float pscale;           // FAST: the one power-of-two scale of every parameter row
+  float pinv;             // 1 / pscale
 };
 
 enum KernelId : int {
@@ -37,7 +40,15 @@ enum KernelId : int {
   K_TOPM_COMBINE, K_LL_TOTAL, K_TOPM_1_1_2, K_TOPM_1_2_2, K_TOPM_2_1_1,
   K_THRESH_COUNT, K_THRESH_SCAN, K_THRESH_SCATTER,
   K_TIED_PREP, K_GRAM_BF16, K_GRAM_F32, K_GRAM_REDUCE, K_SIGMA_TIED, K_GRAM_REDUCE_F32,
+  K_BMAX,
 };
+
+// Handles of the two-team FAST EM kernels (em_fast.cu), nch = 1 or 2, one per
+// mode (MODE_EM, MODE_LSE, MODE_GIVEN), and their dynamic shared-memory size
+// (512 threads per CTA).
+const void* emfast_handle(int nch, int mode);
+size_t emfast_smem(int nch);
+constexpr int kEmFastThreads = 512;
 
 // Threshold assignment: points per block of the count and scatter kernels.
 constexpr int kThreshBlock = 256;
@@ -68,6 +79,7 @@ struct FusedArgs {
   int topm;            // m of the top-m mode
   int topm_max;        // m rounded up to a power of two (2..16): candidate list length
   const uint8_t* p_img;   // parameter operand images, one per slice
+  const uint8_t* c_img;   // FAST: the logit constants as a 128 x 16 operand, one per slice
   const float* cadj;      // per-component logit constant (log2 units)
   const float* iscale;    // per-component scale of the logit accumulator
   const Meta* meta;

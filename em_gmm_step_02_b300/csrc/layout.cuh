@@ -27,4 +27,21 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c16)
   return (r >> 3) * 1024u + (r & 7u) * 128u + ((c16 ^ (r & 7u)) << 4);
 }
 
+// The logit constant enters the logit contraction as one more 16-wide K step:
+// an operand of 128 rows x 16 columns without swizzling (8-row x 16-byte core
+// matrices; the two core matrices of a row group sit 128 bytes apart along K,
+// row groups 256 bytes apart).  The data side of that step is the same in
+// every row: 2^15, 2^4, 2^-7 in columns 0..2 and zeros elsewhere; the
+// parameter side holds, per component, the constant split into three fp16
+// pieces scaled by 2^-15, 2^-4 and 2^7, so that the products add up to it.
+constexpr int kConstBytes = 128 * 16 * 2;   // 4 KB
+constexpr uint32_t kConstLbo = 128;
+constexpr uint32_t kConstSbo = 256;
+__host__ __device__ constexpr int const_exp(int i) { return i == 0 ? 15 : i == 1 ? 4 : -7; }
+
+// Byte offset of element (row, k) of a 128 x 16 operand in that layout.
+__host__ __device__ __forceinline__ uint32_t const_off(uint32_t row, uint32_t k) {
+  return (row >> 3) * kConstSbo + (k >> 3) * kConstLbo + (row & 7u) * 16u + (k & 7u) * 2u;
+}
+
 }  // namespace gmm

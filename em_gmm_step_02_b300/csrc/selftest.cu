@@ -17,6 +17,8 @@ constexpr int kOperandBytes = 64 * 1024;  // each operand buffer
 // variant bit 0: 0 = both operands K-major (M=128, N=128, K=64)
 //                1 = both operands MN-major (M=128, N=256, K=64)
 // variant bit 1: 0 = fp16, 1 = bf16
+// variant 4:     both operands K-major without swizzling (the layout of the
+//                logit constant step), fp16, M=128, N=128, K=16
 __global__ void __launch_bounds__(128, 1)
 selftest_mma_kernel(int variant, const uint4* __restrict__ a_img, const uint4* __restrict__ b_img,
                     float* __restrict__ d_out, uint32_t* __restrict__ status) {
@@ -29,11 +31,12 @@ selftest_mma_kernel(int variant, const uint4* __restrict__ a_img, const uint4* _
   __shared__ uint32_t abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool mn = (variant & 1) != 0;
-  const uint32_t ab_type = (variant >> 1) & 1;
+  const bool nosw = variant == 4;
+  const bool mn = !nosw && (variant & 1) != 0;
+  const uint32_t ab_type = nosw ? 0u : (variant >> 1) & 1;
   const int N = mn ? 256 : 128;
-  const int a_bytes = mn ? 16384 : 16384;   // 64 x 128 or 128 x 64 sixteen-bit elements
-  const int b_bytes = mn ? 32768 : 16384;
+  const int a_bytes = nosw ? kConstBytes : 16384;   // 64 x 128 or 128 x 64 sixteen-bit elements
+  const int b_bytes = nosw ? kConstBytes : (mn ? 32768 : 16384);
 
   for (int i = tid; i < a_bytes / 16; i += 128) reinterpret_cast<uint4*>(sa)[i] = a_img[i];
   for (int i = tid; i < b_bytes / 16; i += 128) reinterpret_cast<uint4*>(sb)[i] = b_img[i];
@@ -50,7 +53,11 @@ selftest_mma_kernel(int variant, const uint4* __restrict__ a_img, const uint4* _
 
   if (tid == 0) {
     const uint32_t idesc = idesc_f16(ab_type, mn ? 1u : 0u, mn ? 1u : 0u, 128, N);
-    for (int k = 0; k < 4; ++k) {
+    if (nosw) {
+      mma_f16_ss(tmem, sdesc_none(smem_u32(sa), kConstLbo, kConstSbo), sdesc_none(smem_u32(sb), kConstLbo, kConstSbo),
+                 idesc, 0);
+    }
+    for (int k = 0; k < (nosw ? 0 : 4); ++k) {
       uint64_t ad, bd;
       if (!mn) {
         ad = sdesc_sw128(smem_u32(sa) + 32u * k, 16, 1024);

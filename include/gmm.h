@@ -258,6 +258,22 @@ const char *gmm_last_error(void);
 /* Free the internal workspace of every device (call when idle). */
 void gmm_release(void);
 
+/* Launch plan of an EM step with these arguments on the current device (for
+ * measurement and tests; no work is enqueued).  Fills info[0..7]:
+ *   [0] CTAs per thread-block cluster (component slices sharing a point tile)
+ *   [1] tile groups of the statistics pass (co-resident clusters, or CTAs per
+ *       slice in the two-pass plan)
+ *   [2] 1 when the step takes two passes (K > 1024, or plan SPLIT)
+ *   [3] tile groups of the normaliser pass (two-pass plan; else 0)
+ *   [4] tiles between flushes of the statistics from tensor memory
+ *   [5] threads per CTA of the E-step kernel
+ *   [6] tile groups gmm_em_step_noalloc would use (its scratch array holds the
+ *       per-group statistics; 0 where that entry point refuses the shape)
+ *   [7] 128-point tiles of the data set
+ * info is a host array of at least 8 int32.  Returns GMM_OK or an error code. */
+int gmm_plan_info(int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
+                  const gmm_opts *opts, int32_t *info);
+
 /* Number of kernel launches the last successful call enqueued. */
 int32_t gmm_last_launch_count(void);
 

@@ -51,3 +51,39 @@ def params_to_device(lw, mu, var, device="cuda"):
     return (torch.tensor(np.asarray(lw, np.float32), device=device),
             torch.tensor(np.asarray(mu, np.float32), device=device),
             torch.tensor(np.asarray(var, np.float32), device=device))
+
+
+# ------------------------------------------------------------------ element-wise parity
+# Relative error is taken element by element.  Each quantity gets the floor of
+# its denominator from the scale on which the arithmetic resolves it:
+#   weights    relative to pi_k (a dead component, pi = 0, must stay 0);
+#   means      relative to max(|mu_kd|, sigma_kd): a coordinate is compared on
+#              the larger of its own size and the component's spread in that
+#              dimension (a mean coordinate near zero has no relative digits,
+#              and EM moves means in units of sigma);
+#   variances  relative to s2_kd, or, where s2_kd is tiny against the raw
+#              second moment m2_kd = s2_kd + mu_kd^2, within four rounding
+#              units (EPS[path]) of m2_kd: the one-pass M-step forms
+#              s2 = m2 - mu^2 from operands carrying EPS relative precision.
+EPS = {"fast": 2.0 ** -12, "precise": 2.0 ** -23}
+
+
+def elementwise_errors(got, ref, cov, path, tol):
+    """(weights, means, variances) error maxima of one EM step, each already
+    divided by its allowed bound (pass: <= 1), plus a description."""
+    lw_g, mu_g, var_g = [np.asarray(a, np.float64) for a in got[:3]]
+    lw_r, mu_r, var_r = [np.asarray(a, np.float64) for a in ref[:3]]
+    K, D = mu_r.shape
+    w_g, w_r = np.exp(lw_g), np.exp(lw_r)
+    e_w = np.abs(w_g - w_r) / np.maximum(w_r, 1e-6 * w_r.max()) / tol
+    v_r = var_r.reshape(K, -1)
+    v_g = var_g.reshape(K, -1)
+    sig = np.sqrt(np.broadcast_to(v_r, (K, D)))
+    e_mu = np.abs(mu_g - mu_r) / np.maximum(np.abs(mu_r), sig) / tol
+    m2 = v_r + (mu_r ** 2 if v_r.shape[1] == D else (mu_r ** 2).mean(1, keepdims=True))
+    bound = np.maximum(tol * v_r, 4.0 * EPS[path] * m2)
+    e_v = np.abs(v_g - v_r) / bound
+    worst = np.unravel_index(np.argmax(e_v), e_v.shape)
+    msg = (f"w {e_w.max() * tol:.2e} mu {e_mu.max() * tol:.2e} var {e_v.max():.2e}x bound "
+           f"(worst k={worst[0]}: ref {v_r[worst]:.3e} got {v_g[worst]:.3e} m2 {m2[worst]:.3e})")
+    return e_w.max(), e_mu.max(), e_v.max(), msg
