@@ -61,6 +61,7 @@ struct FastSmall {
   uint64_t acc2_empty;       // statistics read out (the 128 threads of the flushing team)
   uint64_t xready[2];        // team t's receive slot filled by every CTA of the cluster
   uint64_t xfree[2];         // team t's slot in every CTA read (4 warps x C CTAs)
+  uint64_t cready[2];        // MODE_TOPM: candidate lists of team t's rows received from every CTA
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -322,6 +323,259 @@ __device__ __forceinline__ void team_loop(const FusedArgs& a, uint8_t* sm, FastS
   }
 }
 
+
+
+// a, b: ascending lists of MAXM keys.  Leaves in a the MAXM smallest of the
+// two, ascending: a[i] = min(a[i], b[MAXM - 1 - i]) is a bitonic sequence that
+// holds them, which half-cleaners of stride MAXM/2, ..., 1 then sort.
+template <int MAXM>
+__device__ __forceinline__ void bitonic_keep_min(float (&a)[MAXM], const float (&b)[MAXM]) {
+#pragma unroll
+  for (int i = 0; i < MAXM; ++i) a[i] = fminf(a[i], b[MAXM - 1 - i]);
+#pragma unroll
+  for (int stride = MAXM / 2; stride >= 1; stride >>= 1)
+#pragma unroll
+    for (int i = 0; i < MAXM; ++i)
+      if ((i & stride) == 0) {
+        const float lo = fminf(a[i], a[i + stride]);
+        const float hi = fmaxf(a[i], a[i + stride]);
+        a[i] = lo;
+        a[i + stride] = hi;
+      }
+}
+
+// ------------------------------------------------------------------ top-m teams
+// MODE_TOPM: each point's m largest responsibilities (over every component of
+// the launch's K group) and their components, best first, ties to the lower
+// index ("Flash-GMM", conclusion: multi-assignment read off the final
+// responsibilities).  Per tile and row (team thread):
+//   1. all 128 logits of the slice from tensor memory, the row maximum M, the
+//      local normaliser, and the slice's MAXM best candidates, ranked by a key
+//      (M - logit with its low seven bits replaced by the column: the order of
+//      keys is the order of logits, equal truncated values fall back to the
+//      lower column; truncation moves a logit by at most 2^-16 of its distance
+//      to M);
+//   2. the normaliser goes to every CTA of the cluster, the candidates (logit
+//      in log2 units, component) to the CTA that finalises the row
+//      (rank = row mod C);
+//   3. the finalising CTA merges the C sorted lists and writes 2^(logit - lse)
+//      and the components (one K group), or the group's best logits and its
+//      normaliser (several K groups, merged by topm_combine_kernel).
+// The candidate lists live in the R area (no statistics in this mode).
+template <typename CF, int MAXM>
+__device__ __forceinline__ void topm_team_loop(const FusedArgs& a, uint8_t* sm, FastSmall* S,
+                                               volatile uint32_t* abort_flag, int t, int warp, int lane, int rank,
+                                               int C, int tgroup, int n_tgroups, int my_tiles, uint32_t tmem,
+                                               int kbase) {
+  const int q = warp & 3;
+  const int nl = 32 * q + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
+  const uint32_t acc = tmem + CF::kAccCol + 128u * static_cast<uint32_t>(t);
+  const float is = a.meta->pinv;
+  const int rpc = kBN / C;                     // rows each CTA finalises
+  const bool mine = (nl % C) == rank;
+  const int m = a.topm;
+  // candidate lists of team t: [source rank][row slot][MAXM] x (logit bits, component)
+  uint8_t* cand = sm + CF::kOffR + t * (kBN * MAXM * 8);
+  double ll = 0.0;
+  float llf = 0.f;
+  for (int j = t; j < my_tiles; j += 2) {
+    const int jj = j >> 1;
+    const int64_t n = static_cast<int64_t>(tgroup + j * n_tgroups) * kBN + nl;
+    const bool valid = n < a.N;
+    // pass 1: the row maximum
+    float M;
+    mbar_wait(&S->acc_full[t], static_cast<uint32_t>(jj & 1), abort_flag, a.status);
+    tc_fence_after();
+    {
+      float v[128];
+      tmem_ld32(acc + lane_off + 0, *reinterpret_cast<float(*)[32]>(v));
+      tmem_ld32(acc + lane_off + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+      tmem_ld32(acc + lane_off + 64, *reinterpret_cast<float(*)[32]>(v + 64));
+      tmem_ld32(acc + lane_off + 96, *reinterpret_cast<float(*)[32]>(v + 96));
+      tmem_wait_ld();
+      float mq[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+      for (int e = 4; e < 128; e += 4) {
+        mq[0] = fmaxf(mq[0], v[e]);
+        mq[1] = fmaxf(mq[1], v[e + 1]);
+        mq[2] = fmaxf(mq[2], v[e + 2]);
+        mq[3] = fmaxf(mq[3], v[e + 3]);
+      }
+      M = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+    }
+    // pass 2, one 32-column chunk at a time (a loop, to keep the code small):
+    // the normaliser's sum, and the slice's MAXM best keys in four independent
+    // streams (column 32 c + e goes to stream e & 3) whose sorted lists are
+    // then merged by bitonic networks; keys ascend, so the lists hold the
+    // smallest keys = largest logits
+    float key[4][MAXM];
+#pragma unroll
+    for (int st = 0; st < 4; ++st)
+#pragma unroll
+      for (int s = 0; s < MAXM; ++s) key[st][s] = __uint_as_float(0x7f7fffffu);
+    const bool live = M > -CUDART_INF_F;
+    const float off = live ? kLog2R - M * is : 0.f;
+    float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float v[32];
+      tmem_ld32(acc + lane_off + 32 * c, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        if (live) sq[e & 3] += ex2(fmaf(v[e], is, off));
+        const float d = live ? fminf(M - v[e], 1e30f) : 1e30f;
+        float x = __uint_as_float((__float_as_uint(d) & ~127u) | static_cast<uint32_t>(32 * c + e));
+#pragma unroll
+        for (int s = 0; s < MAXM; ++s) {
+          const float lo = fminf(x, key[e & 3][s]);
+          x = fmaxf(x, key[e & 3][s]);
+          key[e & 3][s] = lo;
+        }
+      }
+    }
+    // the logit buffer is free for tile j + 2
+    tc_fence_before();
+    mbar_arrive(&S->acc_empty[t]);
+    const float ssum = (sq[0] + sq[1]) + (sq[2] + sq[3]);
+    const float lse_loc = ssum > 0.f ? M * is + lg2(ssum) - kLog2R : -CUDART_INF_F;
+    if (C > 1) {
+      if (jj > 0) mbar_wait_cluster(&S->xfree[t], static_cast<uint32_t>((jj - 1) & 1), abort_flag, a.status);
+      const uint32_t dst = smem_u32(&S->xrecv[t][rank][nl]);
+      const uint32_t bar = smem_u32(&S->xready[t]);
+      for (int r = 0; r < C; ++r) st_async_f32(mapa(dst, r), lse_loc, mapa(bar, r));
+      if (q == 0 && lane == 0) {
+        mbar_arrive_expect_tx(&S->xready[t], static_cast<uint32_t>(C * kBN * 4));
+        mbar_arrive_expect_tx(&S->cready[t], static_cast<uint32_t>(kBN * MAXM * 8));
+      }
+    }
+    bitonic_keep_min<MAXM>(key[0], key[1]);
+    bitonic_keep_min<MAXM>(key[2], key[3]);
+    bitonic_keep_min<MAXM>(key[0], key[2]);
+    // candidates in log2 units with their components
+    float cv[MAXM];
+    uint32_t ci[MAXM];
+#pragma unroll
+    for (int s = 0; s < MAXM; ++s) {
+      const uint32_t b = __float_as_uint(key[0][s]);
+      const float dd = __uint_as_float(b & ~127u);
+      cv[s] = dd >= 1e29f ? -CUDART_INF_F : (M - dd) * is;
+      ci[s] = static_cast<uint32_t>(kbase) + (b & 127u);
+    }
+    float lse = lse_loc;
+    if (C > 1) {
+      const int fin = nl % C;
+      const uint32_t cdst = smem_u32(cand + ((rank * rpc + nl / C) * MAXM) * 8);
+      const uint32_t cbar = mapa(smem_u32(&S->cready[t]), static_cast<uint32_t>(fin));
+#pragma unroll
+      for (int s = 0; s < MAXM; ++s)
+        st_async_v2(mapa(cdst + 8u * s, static_cast<uint32_t>(fin)), __float_as_uint(cv[s]), ci[s], cbar);
+      mbar_wait_cluster(&S->xready[t], static_cast<uint32_t>(jj & 1), abort_flag, a.status);
+      float vals[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) vals[r] = r < C ? S->xrecv[t][r][nl] : -CUDART_INF_F;
+      float mx = vals[0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r) mx = fmaxf(mx, vals[r]);
+      float s2 = 0.f;
+      if (mx > -CUDART_INF_F) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) s2 += ex2(vals[r] - mx);
+      }
+      lse = s2 > 0.f ? mx + lg2(s2) : -CUDART_INF_F;
+      mbar_wait_cluster(&S->cready[t], static_cast<uint32_t>(jj & 1), abort_flag, a.status);
+      if (mine) {
+        // C-way merge of the sorted lists of this row (the lists' heads in
+        // registers, the next entry of the list that gave the output read back)
+        float hv[8];
+        uint32_t hi[8];
+        int hp[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          hp[r] = 0;
+          if (r < C) {
+            const uint2 w = *reinterpret_cast<const uint2*>(cand + ((r * rpc + nl / C) * MAXM) * 8);
+            hv[r] = __uint_as_float(w.x);
+            hi[r] = w.y;
+          } else {
+            hv[r] = -CUDART_INF_F;
+            hi[r] = 0xFFFFFFFFu;
+          }
+        }
+#pragma unroll
+        for (int s = 0; s < MAXM; ++s) {
+          if (s < m) {
+            int best = 0;
+            float bv = hv[0];
+            uint32_t bi = hi[0];
+#pragma unroll
+            for (int r = 1; r < 8; ++r)
+              if (hv[r] > bv || (hv[r] == bv && hi[r] < bi)) {
+                best = r;
+                bv = hv[r];
+                bi = hi[r];
+              }
+            cv[s] = bv;
+            ci[s] = bi;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+              if (r == best) {
+                ++hp[r];
+                if (hp[r] < MAXM) {
+                  const uint2 w = *reinterpret_cast<const uint2*>(cand + ((r * rpc + nl / C) * MAXM + hp[r]) * 8);
+                  hv[r] = __uint_as_float(w.x);
+                  hi[r] = w.y;
+                } else {
+                  hv[r] = -CUDART_INF_F;
+                  hi[r] = 0xFFFFFFFFu;
+                }
+              }
+            }
+          }
+        }
+      }
+      // this warp has read its slot rows and candidate lists
+      __syncwarp();
+      if (lane < C) mbar_arrive_remote_relaxed(mapa(smem_u32(&S->xfree[t]), static_cast<uint32_t>(lane)));
+    }
+    if (mine && valid) {
+      if (a.topm_groups == 1) {
+        llf += lse;
+#pragma unroll
+        for (int s = 0; s < MAXM; ++s) {
+          if (s < m) {
+            a.topm_val[n * m + s] = lse > -CUDART_INF_F ? ex2(cv[s] - lse) : 0.f;
+            a.topm_idx[n * m + s] = static_cast<int32_t>(ci[s]);
+          }
+        }
+      } else {
+        a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
+        const int64_t o = (static_cast<int64_t>(blockIdx.y) * a.N + n) * m;
+#pragma unroll
+        for (int s = 0; s < MAXM; ++s) {
+          if (s < m) {
+            a.topm_val[o + s] = cv[s];
+            a.topm_idx[o + s] = static_cast<int32_t>(ci[s]);
+          }
+        }
+      }
+    }
+  }
+  // log-likelihood partial of this CTA (one K group)
+  if (a.topm_groups == 1) {
+    ll += static_cast<double>(llf);
+    for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, o);
+    if (lane == 0) S->ll_red[warp - 4] = ll;
+    named_bar_sync(1, 256);
+    if (warp == 4 && lane == 0) {
+      double tot = 0.0;
+      for (int i = 0; i < 8; ++i) tot += S->ll_red[i];
+      a.ll_part[tgroup * C + rank] = tot * kLn2;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ S0 warps
 // Warp 13 + h sums components 64 h + 2 lane and + 1 of every R quarter (fp32,
 // the same fp16 values the statistics MMA reads) and adds the sums to the
@@ -436,7 +690,7 @@ __device__ __forceinline__ void mma_loop(const FusedArgs& a, uint8_t* sm, FastSm
 }
 
 // ------------------------------------------------------------------ kernel
-template <int NCH, int MODE>
+template <int NCH, int MODE, int MAXM>
 __global__ void __launch_bounds__(512, 1) em_fast_kernel(const FusedArgs a) {
   using CF = FastCfg<NCH>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -483,6 +737,7 @@ __global__ void __launch_bounds__(512, 1) em_fast_kernel(const FusedArgs a) {
       }
       mbar_init(&S->xready[i], 1);
       mbar_init(&S->xfree[i], 4 * C);
+      mbar_init(&S->cready[i], 1);
     }
     mbar_init(&S->p_full, 1);
     mbar_init(&S->acc2_full[0], 1);
@@ -518,7 +773,12 @@ __global__ void __launch_bounds__(512, 1) em_fast_kernel(const FusedArgs a) {
     else transform_warps<CF, FastSmall, 1, NCH, 2, false, false>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
   } else if (wg <= 2) {
     regs_claim<160>();
-    team_loop<CF, MODE>(a, sm, S, abort_flag, wg - 1, warp, lane, rank, C, tgroup, n_tgroups, my_tiles, tmem, kbase, kvalid);
+    if constexpr (MODE == MODE_TOPM)
+      topm_team_loop<CF, MAXM>(a, sm, S, abort_flag, wg - 1, warp, lane, rank, C, tgroup, n_tgroups, my_tiles, tmem,
+                               kbase);
+    else
+      team_loop<CF, MODE>(a, sm, S, abort_flag, wg - 1, warp, lane, rank, C, tgroup, n_tgroups, my_tiles, tmem, kbase,
+                          kvalid);
   } else {
     regs_release<72>();
     if (warp == 12) {
@@ -555,15 +815,21 @@ __global__ void __launch_bounds__(512, 1) em_fast_kernel(const FusedArgs a) {
 
 }  // namespace
 
-const void* emfast_handle(int nch, int mode) {
-  if (nch == 1) {
-    if (mode == MODE_LSE) return reinterpret_cast<const void*>(&em_fast_kernel<1, MODE_LSE>);
-    if (mode == MODE_GIVEN) return reinterpret_cast<const void*>(&em_fast_kernel<1, MODE_GIVEN>);
-    return reinterpret_cast<const void*>(&em_fast_kernel<1, MODE_EM>);
+template <int NCH>
+const void* emfast_handle_nch(int mode, int maxm) {
+  switch (mode) {
+    case MODE_LSE: return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_LSE, 0>);
+    case MODE_GIVEN: return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_GIVEN, 0>);
+    case MODE_TOPM:
+      if (maxm <= 2) return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_TOPM, 2>);
+      if (maxm <= 4) return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_TOPM, 4>);
+      return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_TOPM, 8>);
+    default: return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_EM, 0>);
   }
-  if (mode == MODE_LSE) return reinterpret_cast<const void*>(&em_fast_kernel<2, MODE_LSE>);
-  if (mode == MODE_GIVEN) return reinterpret_cast<const void*>(&em_fast_kernel<2, MODE_GIVEN>);
-  return reinterpret_cast<const void*>(&em_fast_kernel<2, MODE_EM>);
+}
+
+const void* emfast_handle(int nch, int mode, int maxm) {
+  return nch == 1 ? emfast_handle_nch<1>(mode, maxm) : emfast_handle_nch<2>(mode, maxm);
 }
 
 size_t emfast_smem(int nch) {

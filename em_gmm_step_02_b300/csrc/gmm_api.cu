@@ -61,7 +61,7 @@ struct Plan {
   int F;
   int flush;
   size_t smem;        // dynamic shared memory of the E-step kernel
-  bool emfast;        // FAST E-step passes run the two-team kernel (em_fast.cu)
+  bool emfast;        // the E-step passes run the two-team kernel (em_fast.cu): FAST, two-pass plan
   int threads;        // threads per CTA of the E-step kernel
   // workspace offsets
   size_t off_meta, off_pimg, off_cimg, off_cadj, off_iscale, off_part, off_llpart, off_lsepart, off_lse, off_ll;
@@ -180,11 +180,11 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   if (p.two_pass && !split) p.n_slices = (p.n_slices + 7) / 8 * 8;   // whole 8-slice groups for pass 1
   p.K_pad = p.n_slices * kSlice;
   p.n_tiles = static_cast<int>((N + kBN - 1) / kBN);
-  p.emfast = p.fast;
+  p.emfast = p.fast && p.two_pass;
   p.smem = p.emfast ? emfast_smem(p.nch) : fused_smem(p.np, p.nch, p.nst);
   p.threads = p.emfast ? kEmFastThreads : 416;
   p.F = 2 * p.nch * kAtomElems + 1;
-  p.flush = p.fast ? 256 : 16;
+  p.flush = p.fast ? 128 : 16;
   const int sms = need_device ? device_sms() : 148;
   const void* fn = p.emfast ? emfast_handle(p.nch, p.two_pass ? MODE_LSE : MODE_EM) : fused_fn(p.np, p.nch, p.nst);
   if (!p.two_pass) {
@@ -197,7 +197,9 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
     p.C = p.C1;
     p.n_kgroups = p.n_slices / p.C1;
     int mc = p.C1 == 1 ? sms : (need_device ? max_clusters(fn, p.smem, p.C1, p.threads) : std::max(1, sms / p.C1));
-    p.tg1 = std::max(1, std::min(p.n_tiles, mc / p.n_kgroups));
+    // every K group gets as many tile groups as clusters can be resident at
+    // once; the groups run one after another in waves, each keeping the GPU full
+    p.tg1 = std::max(1, std::min(p.n_tiles, mc));
     p.tg = std::max(1, std::min(p.n_tiles, sms / p.n_slices));
   }
   // workspace layout
@@ -630,14 +632,34 @@ TopmSpace topm_space(const Plan& p, int m, size_t base) {
   return t;
 }
 
+// FAST top-m runs on the two-team kernel when its candidate lists fit the
+// R area: lists of at most 8 and a cluster size that divides the 128 rows.
+bool topm_two_team(const Plan& p, int m) {
+  const int C = p.two_pass ? p.C1 : p.C;
+  return p.fast && m <= 8 && (C == 1 || C == 2 || C == 4 || C == 8);
+}
+
+const void* topm_fn(const Plan& p, int m) {
+  const int maxm = m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
+  return topm_two_team(p, m) ? emfast_handle(p.nch, MODE_TOPM, maxm) : fused_fn(p.np, p.nch, p.nst, true);
+}
+
+size_t topm_smem(const Plan& p, int m) {
+  return topm_two_team(p, m) ? emfast_smem(p.nch) : fused_smem(p.np, p.nch, p.nst);
+}
+
 // The top-m pass over X: each point's m largest responsibilities and their
 // components into resp_out / idx_out (N x m, device); the total
 // log-likelihood into ll_dev when it is not NULL.
 int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_out, double* ll_dev, uint8_t* ws,
              const TopmSpace& ts, cudaStream_t s) {
   const int maxm = m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
-  const void* fn = fused_fn(p.np, p.nch, p.nst, true);
-  const size_t smem = fused_smem(p.np, p.nch, p.nst);
+  const int C = p.two_pass ? p.C1 : p.C;
+  const bool team = topm_two_team(p, m);
+  const void* fn = team ? emfast_handle(p.nch, MODE_TOPM, maxm) : fused_fn(p.np, p.nch, p.nst, true);
+  const size_t smem = team ? emfast_smem(p.nch) : fused_smem(p.np, p.nch, p.nst);
+  const int threads = team ? kEmFastThreads : 416;
+  (void)C;
   FusedArgs a = base_args(p, X, ws);
   a.mode = MODE_TOPM;
   a.topm = m;
@@ -649,7 +671,7 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
     a.topm_groups = 1;
     a.topm_val = resp_out;
     a.topm_idx = idx_out;
-    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(416), smem, s, p.C, a))) return r;
+    if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(threads), smem, s, p.C, a))) return r;
     if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
                               static_cast<const double*>(a.ll_part), p.tg * p.C, ll_dev)))
       return r;
@@ -658,7 +680,7 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
     a.topm_groups = p.n_kgroups;
     a.topm_val = reinterpret_cast<float*>(ws + ts.off_gval);
     a.topm_idx = reinterpret_cast<int32_t*>(ws + ts.off_gidx);
-    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(416), smem, s, p.C1, a))) return r;
+    if ((r = launch_main(fn, dim3(p.C1 * p.tg1, p.n_kgroups), dim3(threads), smem, s, p.C1, a))) return r;
     if ((r = launch(kernel_handle(K_TOPM_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
                     static_cast<const float*>(a.lse_part), static_cast<const float*>(a.topm_val),
                     static_cast<const int32_t*>(a.topm_idx), p.n_kgroups, p.N, m, resp_out, idx_out,
@@ -844,7 +866,7 @@ int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = nullptr;
   if ((r = get_workspace(ts.end, &ws))) return r;
-  if ((r = set_smem_attr(fused_fn(p.np, p.nch, p.nst, true), fused_smem(p.np, p.nch, p.nst)))) return r;
+  if ((r = set_smem_attr(topm_fn(p, m), topm_smem(p, m)))) return r;
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
   double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
   if ((r = run_topm(p, X, m, resp_out, idx_out, ll_dev, ws, ts, s))) return r;
@@ -887,7 +909,7 @@ int gmm_assign_threshold(const void* X, int64_t N, int32_t D, int32_t K, int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = nullptr;
   if ((r = get_workspace(ts.end, &ws))) return r;
-  if ((r = set_smem_attr(fused_fn(p.np, p.nch, p.nst, true), fused_smem(p.np, p.nch, p.nst)))) return r;
+  if ((r = set_smem_attr(topm_fn(p, m), topm_smem(p, m)))) return r;
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
   float* tr = reinterpret_cast<float*>(ws + off_r);
   int32_t* ti = reinterpret_cast<int32_t*>(ws + off_i);

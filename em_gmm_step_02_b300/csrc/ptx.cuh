@@ -170,6 +170,14 @@ __device__ __forceinline__ void st_async_f32(uint32_t caddr, float v, uint32_t c
                :: "r"(caddr), "r"(__float_as_uint(v)), "r"(cbar) : "memory");
 }
 
+// Store two 32-bit words (8 bytes, 8-byte aligned) into shared memory of a
+// CTA of the cluster and signal 8 transaction bytes on the mbarrier at cluster
+// address cbar (in the same CTA as caddr).
+__device__ __forceinline__ void st_async_v2(uint32_t caddr, uint32_t a, uint32_t b, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+               :: "r"(caddr), "r"(a), "r"(b), "r"(cbar) : "memory");
+}
+
 // Bulk copy of `bytes` from this CTA's shared memory (src) to shared memory
 // of a CTA of the cluster (cluster address dst), completing `bytes`
 // transaction bytes on the mbarrier at cluster address cbar (in the
