@@ -39,7 +39,8 @@ class GmmError(RuntimeError):
 class gmm_opts(ctypes.Structure):
     _fields_ = [("precision", ctypes.c_int32), ("reg_covar", ctypes.c_float),
                 ("var_floor", ctypes.c_float), ("x_absmax", ctypes.c_float),
-                ("loglik_on_host", ctypes.c_int32), ("plan", ctypes.c_int32)]
+                ("loglik_on_host", ctypes.c_int32), ("plan", ctypes.c_int32),
+                ("wait_limit", ctypes.c_int32), ("approx_top_k", ctypes.c_int32)]
 
 
 _lib = None

@@ -3,9 +3,8 @@
     python -m em_gmm_step_02_b300.build [--force]
 
 nvcc compiles every ``csrc/*.cu`` for ``-gencode arch=compute_103a,code=sm_103a``
-and links them, with the CUDA runtime (and cuBLAS, for the Gram matrix of bf16
-data in the tied-covariance model: a plain batched GEMM), into one shared
-library whose C ABI is ``include/gmm.h``.  Object files go to ``_build/`` at the repository root.
+and links them with the CUDA runtime into one shared library whose C ABI is
+``include/gmm.h``.  Object files go to ``_build/`` at the repository root.
 """
 from __future__ import annotations
 
@@ -48,7 +47,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         objs.append(obj)
     tmp = LIB + f".tmp{os.getpid()}"
     subprocess.check_call([NVCC, "-gencode", "arch=compute_103a,code=sm_103a", "-shared",
-                           "-o", tmp, *objs, "-lcudart", "-lcublas"])
+                           "-o", tmp, *objs, "-lcudart"])
     os.replace(tmp, LIB)
     return LIB
 

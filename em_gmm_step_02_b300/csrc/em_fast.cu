@@ -65,6 +65,7 @@ struct FastSmall {
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
+  uint32_t poll_limit;       // follows abort_flag (read by the bounded waits)
 };
 
 // Shared-memory plan: [stage 0 | stage 1 | parameter image | constant operand |
@@ -726,6 +727,7 @@ __global__ void __launch_bounds__(512, 1) em_fast_kernel(const FusedArgs a) {
 
   if (tid == 0) {
     S->abort_flag = 0;
+    S->poll_limit = a.max_polls ? a.max_polls : kMaxPolls;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S->full_a[i], 128);
       for (int g = 0; g < 8; ++g) mbar_init(&S->empty_g[i][g], 1);

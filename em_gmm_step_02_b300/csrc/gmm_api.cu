@@ -1,7 +1,6 @@
 // gmm_api.cu -- host side of the C ABI declared in include/gmm.h: argument
 // checks, the launch plan (precision, cluster size, single or two-pass),
 // the per-device workspace, and the launch sequence of one EM step.
-#include <cublas_v2.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -60,6 +59,7 @@ struct Plan {
   int tg1;            // tile groups of pass 1 (two-pass)
   int F;
   int flush;
+  uint32_t max_polls; // polls per device-side wait (0: the kernels' default)
   size_t smem;        // dynamic shared memory of the E-step kernel
   bool emfast;        // the E-step passes run the two-team kernel (em_fast.cu): FAST, two-pass plan
   int threads;        // threads per CTA of the E-step kernel
@@ -74,8 +74,6 @@ struct Plan {
 };
 
 constexpr int kCombineBlocks = 296;
-// rows per chunk of the bf16 Gram matrix (one GEMM of the batch each)
-constexpr int64_t kGramRows = 8192;
 // default rows per chunk of the host-data entry point (1 GiB of bf16 rows at D = 128)
 constexpr int64_t kHostChunkRows = int64_t(1) << 22;
 constexpr size_t kStatusBytes = 256;
@@ -159,6 +157,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   if (o.precision < GMM_PREC_AUTO || o.precision > GMM_PREC_PRECISE)
     return fail(GMM_ERR_INVALID_ARG, "unknown precision");
   if (o.plan < GMM_PLAN_AUTO || o.plan > GMM_PLAN_SPLIT) return fail(GMM_ERR_INVALID_ARG, "unknown plan");
+  if (o.wait_limit < 0) return fail(GMM_ERR_INVALID_ARG, "wait_limit must be >= 0");
   if (!(o.reg_covar >= 0.f) || !(o.var_floor >= 0.f) || !std::isfinite(o.reg_covar) || !std::isfinite(o.var_floor))
     return fail(GMM_ERR_INVALID_ARG, "reg_covar and var_floor must be finite and >= 0");
   if (!(o.x_absmax >= 0.f) || !std::isfinite(o.x_absmax)) return fail(GMM_ERR_INVALID_ARG, "x_absmax must be finite and >= 0");
@@ -167,6 +166,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   if (N > (int64_t(1) << 40)) return fail(GMM_ERR_UNSUPPORTED, "N too large");
   if (X && (reinterpret_cast<uintptr_t>(X) & 15)) return fail(GMM_ERR_INVALID_ARG, "X must be 16-byte aligned");
   p.N = N; p.D = D; p.K = K; p.cov_diag = cov; p.x_bf16 = dtype == GMM_BF16;
+  p.max_polls = static_cast<uint32_t>(o.wait_limit);
   const int prec = o.precision == GMM_PREC_AUTO ? (p.x_bf16 ? GMM_PREC_FAST : GMM_PREC_PRECISE) : o.precision;
   p.fast = prec == GMM_PREC_FAST;
   p.nch = D <= 64 ? 1 : 2;
@@ -225,7 +225,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.off_tl = p.off_sinv = p.off_twork = p.off_logdet = p.off_gram = p.off_gpart = p.off_tstats = p.off_tsig = off;
   if (p.cov_diag == GMM_TIED) {
     const size_t dd = sizeof(double) * static_cast<size_t>(D) * D;
-    p.n_gram = p.x_bf16 ? static_cast<int>((N + kGramRows - 1) / kGramRows) : 2 * sms;
+    p.n_gram = std::max(1, std::min(p.n_tiles, sms));   // one partial per CTA of the Gram kernel
     p.off_tl = off; off += align256(dd);
     p.off_sinv = off; off += align256(dd);
     p.off_twork = off; off += align256(dd);
@@ -337,58 +337,6 @@ int check_ptr(const void* p, const char* name) {
   return GMM_OK;
 }
 
-// cuBLAS handle per device (the Gram matrix of bf16 data is a plain GEMM).
-std::mutex g_blas_mu;
-std::map<int, cublasHandle_t> g_blas;
-
-int blas_handle(cublasHandle_t* out) {
-  int dev = 0;
-  CUDA_TRY(cudaGetDevice(&dev));
-  std::lock_guard<std::mutex> lk(g_blas_mu);
-  cublasHandle_t& h = g_blas[dev];
-  if (!h && cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) {
-    h = nullptr;
-    return fail(GMM_ERR_CUDA, "cublasCreate failed");
-  }
-  *out = h;
-  return GMM_OK;
-}
-
-// part[b] = X_b^T X_b (D x D, fp32) for the row chunks X_b of kGramRows rows
-// of the row-major bf16 X: one strided batched GEMM (bf16 operands, fp32
-// accumulation) plus one GEMM for a shorter last chunk.  In column-major
-// terms X_b is the D x rows matrix A with leading dimension D, and
-// part[b] = A A^T.
-int gram_bf16(const Plan& p, const void* X, float* part, cudaStream_t s) {
-  cublasHandle_t h = nullptr;
-  int r = blas_handle(&h);
-  if (r) return r;
-  if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return fail(GMM_ERR_CUDA, "cublasSetStream failed");
-  const float one = 1.f, zero = 0.f;
-  const int D = p.D;
-  const int64_t full = p.N / kGramRows;
-  const int64_t rest = p.N - full * kGramRows;
-  const auto* x = static_cast<const __nv_bfloat16*>(X);
-  if (full > 0) {
-    cublasStatus_t st = cublasGemmStridedBatchedEx(
-        h, CUBLAS_OP_N, CUBLAS_OP_T, D, D, static_cast<int>(kGramRows), &one, x, CUDA_R_16BF, D,
-        kGramRows * D, x, CUDA_R_16BF, D, kGramRows * D, &zero, part, CUDA_R_32F, D,
-        static_cast<long long>(D) * D, static_cast<int>(full), CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    if (st != CUBLAS_STATUS_SUCCESS) return fail(GMM_ERR_CUDA, "cublasGemmStridedBatchedEx failed");
-    ++g_launches;
-  }
-  if (rest > 0) {
-    const __nv_bfloat16* xr = x + full * kGramRows * D;
-    cublasStatus_t st = cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, D, D, static_cast<int>(rest), &one, xr,
-                                     CUDA_R_16BF, D, xr, CUDA_R_16BF, D, &zero,
-                                     part + full * static_cast<int64_t>(D) * D, CUDA_R_32F, D,
-                                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    if (st != CUBLAS_STATUS_SUCCESS) return fail(GMM_ERR_CUDA, "cublasGemmEx failed");
-    ++g_launches;
-  }
-  return GMM_OK;
-}
-
 // prep: scan (optional), meta, parameter images
 int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, const float* var,
              const gmm_opts& o, uint8_t* ws, cudaStream_t s) {
@@ -429,20 +377,28 @@ int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, con
                    reinterpret_cast<double*>(ws + p.off_tl), sinv, logdet,
                    reinterpret_cast<double*>(ws + p.off_twork), status);
     if (r) return r;
-    if (X && p.x_bf16) {
-      // bf16 data (FAST: unshifted) on the tensor cores, chunk by chunk
-      if ((r = gram_bf16(p, X, reinterpret_cast<float*>(ws + p.off_gpart), s))) return r;
-      r = launch(kernel_handle(K_GRAM_REDUCE_F32), dim3((p.D * p.D + 255) / 256), dim3(256), 0, s, 1,
-                 static_cast<const float*>(reinterpret_cast<float*>(ws + p.off_gpart)), p.n_gram, p.D,
-                 reinterpret_cast<double*>(ws + p.off_gram));
-      if (r) return r;
-    } else if (X) {
+    if (X) {
+      // G = sum (x - shift)(x - shift)^T on the tensor cores: one CTA per SM,
+      // fp64 partials per CTA, fixed-order reduction
+      const void* gfn = gram_handle(p.np, p.nch, p.x_bf16 != 0);
+      const size_t gsm = gram_smem(p.np, p.nch);
+      if ((r = set_smem_attr(gfn, gsm))) return r;
       double* gpart = reinterpret_cast<double*>(ws + p.off_gpart);
-      r = launch(kernel_handle(K_GRAM_F32), dim3(p.n_gram, p.D > 64 ? 4 : 1), dim3(256),
-                 0, s, 1, X, p.N, p.D, static_cast<const Meta*>(meta), gpart);
-      if (r) return r;
+      CUDA_TRY(cudaMemsetAsync(gpart, 0, sizeof(double) * static_cast<size_t>(p.n_gram) * p.D * p.D, s));
+      FusedArgs ga = {};
+      ga.X = X;
+      ga.N = p.N;
+      ga.D = p.D;
+      ga.x_bf16 = p.x_bf16;
+      ga.n_tiles = p.n_tiles;
+      ga.flush_tiles = p.flush;
+      ga.meta = meta;
+      ga.status = status;
+      ga.max_polls = p.max_polls;
+      if ((r = launch(gfn, dim3(p.n_gram), dim3(gram_threads()), gsm, s, 1, ga, gpart))) return r;
       r = launch(kernel_handle(K_GRAM_REDUCE), dim3((p.D * p.D + 255) / 256), dim3(256), 0, s, 1,
-                 static_cast<const double*>(gpart), p.n_gram, p.D, reinterpret_cast<double*>(ws + p.off_gram));
+                 static_cast<const double*>(gpart), p.n_gram, p.D, static_cast<const Meta*>(meta),
+                 reinterpret_cast<double*>(ws + p.off_gram));
       if (r) return r;
     }
   }
@@ -497,6 +453,7 @@ FusedArgs base_args(const Plan& p, const void* X, uint8_t* ws) {
   a.lse_part = reinterpret_cast<float*>(ws + p.off_lsepart);
   a.lse_in = reinterpret_cast<const float*>(ws + p.off_lse);
   a.status = reinterpret_cast<uint32_t*>(ws);
+  a.max_polls = p.max_polls;
   return a;
 }
 
@@ -699,6 +656,98 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
   return GMM_OK;
 }
 
+// Approximate top-k EM: workspace placed from byte `base` on -- the top-k
+// lists (responsibilities, components) of every point, the counting sort's
+// per-(component, tile) counts, per-component totals and offsets, the sorted
+// pairs, the per-chunk partial statistics and N_k, then the top-m pass's
+// own space.
+struct TopkSpace {
+  int64_t T;            // tiles of kTkTile points
+  int64_t max_chunks;   // bound on the chunks of kTkChunk pairs over all components
+  size_t off_r, off_i, off_cnt, off_tot, off_base, off_cbase, off_pt, off_rw, off_part, off_nk;
+  TopmSpace tm;
+  size_t end;
+};
+TopkSpace topk_space(const Plan& p, int k, size_t base) {
+  TopkSpace t;
+  const size_t nk = static_cast<size_t>(p.N) * k;
+  t.T = (p.N + kTkTile - 1) / kTkTile;
+  t.max_chunks = static_cast<int64_t>(nk / kTkChunk) + p.K + 1;
+  t.off_r = base;
+  t.off_i = t.off_r + align256(sizeof(float) * nk);
+  t.off_cnt = t.off_i + align256(sizeof(int32_t) * nk);
+  t.off_tot = t.off_cnt + align256(sizeof(int32_t) * static_cast<size_t>(p.K) * t.T);
+  t.off_base = t.off_tot + align256(sizeof(int32_t) * p.K);
+  t.off_cbase = t.off_base + align256(sizeof(int64_t) * (p.K + 1));
+  t.off_pt = t.off_cbase + align256(sizeof(int32_t) * (p.K + 1));
+  t.off_rw = t.off_pt + align256(sizeof(uint32_t) * nk);
+  t.off_part = t.off_rw + align256(sizeof(float) * nk);
+  t.off_nk = t.off_part + align256(sizeof(double) * static_cast<size_t>(t.max_chunks) * (p.D + 1));
+  t.tm = topm_space(p, k, t.off_nk + align256(sizeof(double) * p.K));
+  t.end = t.tm.end;
+  return t;
+}
+
+bool approx_topk_on(const gmm_opts& o, int K) { return o.approx_top_k > 0 && o.approx_top_k < K; }
+
+int check_approx_topk(const gmm_opts& o, int64_t N, int K, int cov) {
+  if (o.approx_top_k < 0) return fail(GMM_ERR_INVALID_ARG, "approx_top_k must be >= 0");
+  if (!approx_topk_on(o, K)) return GMM_OK;
+  if (o.approx_top_k > 16) return fail(GMM_ERR_UNSUPPORTED, "approx_top_k must be <= 16 (or >= K for exact EM)");
+  if (cov != GMM_SPHERICAL && cov != GMM_DIAG)
+    return fail(GMM_ERR_UNSUPPORTED, "approx_top_k needs a spherical or diagonal covariance");
+  if (N > 0x7fffffffLL) return fail(GMM_ERR_UNSUPPORTED, "approx_top_k needs N < 2^31");
+  return GMM_OK;
+}
+
+// The M-step of approximate top-k EM from the top-k lists in the workspace
+// (the E-step, run_topm with m = k, has written them).
+int run_topk_mstep(const Plan& p, const void* X, int k, const gmm_opts& o, uint8_t* ws, const TopkSpace& t,
+                   const float* means, const float* vars, float* new_log_weights, float* new_means, float* new_vars,
+                   cudaStream_t s) {
+  int r;
+  const bool xb = p.x_bf16 != 0;
+  int32_t* cnt = reinterpret_cast<int32_t*>(ws + t.off_cnt);
+  int32_t* tot = reinterpret_cast<int32_t*>(ws + t.off_tot);
+  int64_t* base = reinterpret_cast<int64_t*>(ws + t.off_base);
+  int32_t* cbase = reinterpret_cast<int32_t*>(ws + t.off_cbase);
+  uint32_t* pt = reinterpret_cast<uint32_t*>(ws + t.off_pt);
+  float* rw = reinterpret_cast<float*>(ws + t.off_rw);
+  double* part = reinterpret_cast<double*>(ws + t.off_part);
+  double* nk = reinterpret_cast<double*>(ws + t.off_nk);
+  const int32_t* idx = reinterpret_cast<const int32_t*>(ws + t.off_i);
+  const float* resp = reinterpret_cast<const float*>(ws + t.off_r);
+  const unsigned tile_blocks = static_cast<unsigned>((t.T + 7) / 8);
+  const unsigned chunk_blocks = static_cast<unsigned>(t.max_chunks);
+  const int cov_diag = p.cov_diag;
+  CUDA_TRY(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * static_cast<size_t>(p.K) * t.T, s));
+  if ((r = launch(topk_handle(TK_COUNT, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, p.N, k, p.K, t.T, cnt)))
+    return r;
+  if ((r = launch(topk_handle(TK_SCAN, xb), dim3(p.K), dim3(256), 0, s, 1, cnt, t.T, tot))) return r;
+  if ((r = launch(topk_handle(TK_BASE, xb), dim3(1), dim3(1024), 0, s, 1, static_cast<const int32_t*>(tot), p.K,
+                  base, cbase)))
+    return r;
+  if ((r = launch(topk_handle(TK_FILL, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, resp, p.N, k, p.K, t.T, cnt,
+                  static_cast<const int64_t*>(base), pt, rw)))
+    return r;
+  const float* nm = new_means;
+  if ((r = launch(topk_handle(TK_STATS1, xb), dim3(chunk_blocks), dim3(128), 0, s, 1, X, p.D, p.K,
+                  static_cast<const int64_t*>(base), static_cast<const int32_t*>(cbase),
+                  static_cast<const uint32_t*>(pt), static_cast<const float*>(rw), nm, part)))
+    return r;
+  if ((r = launch(topk_handle(TK_FINAL1, xb), dim3(p.K), dim3(128), 0, s, 1, static_cast<const double*>(part),
+                  static_cast<const int32_t*>(cbase), p.N, p.D, cov_diag, o.reg_covar, o.var_floor, means, vars, nk,
+                  new_log_weights, new_means, new_vars)))
+    return r;
+  if ((r = launch(topk_handle(TK_STATS2, xb), dim3(chunk_blocks), dim3(128), 0, s, 1, X, p.D, p.K,
+                  static_cast<const int64_t*>(base), static_cast<const int32_t*>(cbase),
+                  static_cast<const uint32_t*>(pt), static_cast<const float*>(rw), nm, part)))
+    return r;
+  return launch(topk_handle(TK_FINAL2, xb), dim3(p.K), dim3(128), 0, s, 1, static_cast<const double*>(part),
+                static_cast<const int32_t*>(cbase), p.N, p.D, cov_diag, o.reg_covar, o.var_floor, means, vars, nk,
+                new_log_weights, new_means, new_vars);
+}
+
 }  // namespace
 
 // ====================================================================== ABI
@@ -712,6 +761,7 @@ void gmm_default_opts(gmm_opts* o) {
   o->x_absmax = 0.f;
   o->loglik_on_host = 0;
   o->plan = GMM_PLAN_AUTO;
+  o->wait_limit = 0;
 }
 
 const char* gmm_last_error(void) { return g_error.c_str(); }
@@ -728,6 +778,8 @@ size_t gmm_workspace_bytes(int64_t N, int32_t D, int32_t K, int32_t cov_type, in
   bool have_dev = cudaGetDeviceCount(&dev_count) == cudaSuccess && dev_count > 0;
   if (!have_dev) cudaGetLastError();
   if (make_plan(p, nullptr, N, D, K, cov_type, x_dtype, o, have_dev) != GMM_OK) return 0;
+  if (check_approx_topk(o, N, K, cov_type) != GMM_OK) return 0;
+  if (approx_topk_on(o, K)) return topk_space(p, o.approx_top_k, p.ws_bytes).end;
   return p.ws_bytes;
 }
 
@@ -738,8 +790,9 @@ int gmm_reserve(int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dty
   Plan p;
   int r = make_plan(p, nullptr, N, D, K, cov_type, x_dtype, o, true);
   if (r) return r;
+  if ((r = check_approx_topk(o, N, K, cov_type))) return r;
   uint8_t* ws = nullptr;
-  return get_workspace(p.ws_bytes, &ws);
+  return get_workspace(approx_topk_on(o, K) ? topk_space(p, o.approx_top_k, p.ws_bytes).end : p.ws_bytes, &ws);
 }
 
 int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type, int32_t x_dtype,
@@ -756,10 +809,30 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
       (r = check_ptr(new_means, "new_means")) || (r = check_ptr(new_vars, "new_vars")))
     return r;
   if (!total_loglik) return fail(GMM_ERR_INVALID_ARG, "total_loglik is NULL");
+  if ((r = check_approx_topk(o, N, K, cov_type))) return r;
   Plan p;
   if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = nullptr;
+  if (approx_topk_on(o, K)) {
+    // approximate top-k EM: the top-m pass (m = k) into the workspace, then
+    // the sparse M-step
+    const int k = o.approx_top_k;
+    const TopkSpace t = topk_space(p, k, p.ws_bytes);
+    if ((r = get_workspace(t.end, &ws))) return r;
+    if ((r = set_smem_attr(topm_fn(p, k), topm_smem(p, k)))) return r;
+    if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
+    double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
+    if ((r = run_topm(p, X, k, reinterpret_cast<float*>(ws + t.off_r), reinterpret_cast<int32_t*>(ws + t.off_i),
+                      ll_dev, ws, t.tm, s)))
+      return r;
+    if ((r = run_topk_mstep(p, X, k, o, ws, t, means, vars, new_log_weights, new_means, new_vars, s))) return r;
+    if (o.loglik_on_host) {
+      CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
+      return sync_status(ws, s);
+    }
+    return GMM_OK;
+  }
   if ((r = get_workspace(p.ws_bytes, &ws))) return r;
   if ((r = set_estep_attrs(p))) return r;
 
@@ -785,6 +858,8 @@ int gmm_em_step_host(const void* X_host, int64_t N, int32_t D, int32_t K, int32_
   if (!X_host) return fail(GMM_ERR_INVALID_ARG, "X_host is NULL");
   if (!(o.x_absmax > 0.f))
     return fail(GMM_ERR_INVALID_ARG, "gmm_em_step_host needs opts->x_absmax > 0 (a bound on max |X|)");
+  if (o.approx_top_k != 0 && o.approx_top_k < K)
+    return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_host runs exact EM only (approx_top_k must be 0 or >= K)");
   if (cov_type == GMM_TIED) return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_host supports spherical and diagonal covariance");
   if (N < 1) return fail(GMM_ERR_INVALID_ARG, "N must be >= 1");
   if (chunk_rows < 0) return fail(GMM_ERR_INVALID_ARG, "chunk_rows must be >= 0");
@@ -901,6 +976,7 @@ int gmm_assign_threshold(const void* X, int64_t N, int32_t D, int32_t K, int32_t
   if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
   const int m = max_per_point;
   const int64_t n_blocks = (N + kThreshBlock - 1) / kThreshBlock;
+  if (n_blocks > 0x7fffffffLL) return fail(GMM_ERR_UNSUPPORTED, "N too large for gmm_assign_threshold (grid limit)");
   // workspace: the EM workspace, the top-m lists of every point, block totals
   const size_t off_r = p.ws_bytes;
   const size_t off_i = off_r + align256(sizeof(float) * static_cast<size_t>(N) * m);
@@ -1006,15 +1082,6 @@ void gmm_release(void) {
     cudaSetDevice(cur);
   }
   g_pipes.clear();
-  std::lock_guard<std::mutex> lk3(g_blas_mu);
-  for (auto& kv : g_blas) {
-    int cur = 0;
-    cudaGetDevice(&cur);
-    cudaSetDevice(kv.first);
-    if (kv.second) cublasDestroy(kv.second);
-    cudaSetDevice(cur);
-  }
-  g_blas.clear();
 }
 
 }  // extern "C"
@@ -1029,7 +1096,7 @@ void gmm_release(void) {
 // code cannot use the variable's name as a device address; its address on
 // each device is looked up once with cudaGetSymbolAddress (on the first call
 // made with that device current) and cached.
-constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;   // 40 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(24) << 20;   // 24 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
@@ -1064,7 +1131,7 @@ int noalloc_layout(Plan& p) {
                  align256(static_cast<size_t>(p.n_slices) * kConstBytes) + 2 * align256(sizeof(float) * p.K_pad) +
                  align256(sizeof(double) * kCombineBlocks);
   if (fixed + align256(row_bytes) > kNoAllocScratchBytes)
-    return fail(GMM_ERR_UNSUPPORTED, "problem too large for the 40 MiB scratch of gmm_em_step_noalloc");
+    return fail(GMM_ERR_UNSUPPORTED, "problem too large for the 24 MiB scratch of gmm_em_step_noalloc");
   const int tg_fit = static_cast<int>((kNoAllocScratchBytes - fixed) / row_bytes);
   p.tg = std::max(1, std::min(p.tg, tg_fit));
   size_t off = kStatusBytes;
@@ -1102,6 +1169,8 @@ extern "C" int gmm_em_step_noalloc(const void* X, int64_t N, int32_t D, int32_t 
   if (cov_type == GMM_TIED) return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_noalloc supports spherical and diagonal covariance");
   o.plan = GMM_PLAN_CLUSTER;   // the single pass: no N-sized buffer
   Plan p;
+  if (o.approx_top_k != 0 && o.approx_top_k < K)
+    return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_noalloc runs exact EM only (approx_top_k must be 0 or >= K)");
   if ((r = make_plan(p, X, N, D, K, cov_type, x_dtype, o, true))) return r;
   if (p.two_pass)
     return fail(GMM_ERR_UNSUPPORTED, "gmm_em_step_noalloc supports K <= 1024 (larger K needs an N-sized buffer)");

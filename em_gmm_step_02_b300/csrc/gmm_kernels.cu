@@ -733,6 +733,7 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
   // ---- set-up
   if (tid == 0) {
     S->abort_flag = 0;
+    S->poll_limit = a.max_polls ? a.max_polls : kMaxPolls;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S->full_a[i], 128);
       for (int g = 0; g < 8; ++g) mbar_init(&S->empty_g[i][g], 1);
@@ -1123,9 +1124,12 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
           }
         }
       }
-      // drain: all issued MMAs complete before tensor memory is released
+      // every copy and tensor-core operation of this CTA completes before the
+      // tensor memory and shared memory are released (bounded waits that do not
+      // give up early after another wait has failed)
+      mbar_wait_final(&S->p_full, 0, a.status);
       mma_commit(&S->drain);
-      mbar_wait(&S->drain, 0, abort_flag, a.status);
+      mbar_wait_final(&S->drain, 0, a.status);
     }
     __syncwarp();
   }
@@ -1375,96 +1379,16 @@ __global__ void tied_prep_kernel(const float* __restrict__ sigma, int D, double*
   }
 }
 
-// Gram matrix partials: block (bx, tile) accumulates the 64 x 64 tile `tile`
-// of G over rows bx, bx + gridDim.x, ... in chunks of 32 rows (fp32 within a
-// chunk, fp64 across chunks) and writes it to part[bx][D][D].  256 threads,
-// 4 x 4 outputs each.
-template <bool XB>
-__global__ void __launch_bounds__(256) gram_kernel(const void* __restrict__ X, int64_t N, int D,
-                                                   const Meta* __restrict__ meta, double* __restrict__ part) {
-  constexpr int R = 32;
-  __shared__ float As[R][64];
-  __shared__ float Bs[R][64];
-  const int ti = blockIdx.y >> 1, tj = blockIdx.y & 1;
-  const int i0 = 64 * ti, j0 = 64 * tj;
-  const int t = threadIdx.x;
-  const int ri = 4 * (t >> 4), cj = 4 * (t & 15);
-  double acc[4][4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) acc[a][b] = 0.0;
-  const int64_t n_chunks = (N + R - 1) / R;
-  for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
-    __syncthreads();
-    for (int e = t; e < R * 64; e += 256) {
-      const int r = e >> 6, col = e & 63;
-      const int64_t n = c * R + r;
-      float va = 0.f, vb = 0.f;
-      if (n < N) {
-        if (i0 + col < D) {
-          const float x = XB ? __bfloat162float(static_cast<const __nv_bfloat16*>(X)[n * D + i0 + col])
-                             : static_cast<const float*>(X)[n * D + i0 + col];
-          va = x - meta->shift[i0 + col];
-        }
-        if (j0 + col < D) {
-          const float x = XB ? __bfloat162float(static_cast<const __nv_bfloat16*>(X)[n * D + j0 + col])
-                             : static_cast<const float*>(X)[n * D + j0 + col];
-          vb = x - meta->shift[j0 + col];
-        }
-      }
-      As[r][col] = va;
-      Bs[r][col] = vb;
-    }
-    __syncthreads();
-    float f[4][4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) f[a][b] = 0.f;
-    for (int r = 0; r < R; ++r) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) av[a] = As[r][ri + a];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) bv[b] = Bs[r][cj + b];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) f[a][b] = fmaf(av[a], bv[b], f[a][b]);
-    }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] += static_cast<double>(f[a][b]);
-  }
-  double* out = part + static_cast<int64_t>(blockIdx.x) * D * D;
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int i = i0 + ri + a, j = j0 + cj + b;
-      if (i < D && j < D) out[static_cast<int64_t>(i) * D + j] = acc[a][b];
-    }
-}
-
-// G = sum over float32 partials (the Gram matrices of row chunks from the
-// batched GEMM of bf16 data), in a fixed order, in fp64.
-__global__ void gram_reduce_f32_kernel(const float* __restrict__ part, int n_parts, int D, double* __restrict__ G) {
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (e >= static_cast<int64_t>(D) * D) return;
-  double s = 0.0;
-  for (int p = 0; p < n_parts; ++p) s += static_cast<double>(part[static_cast<int64_t>(p) * D * D + e]);
-  G[e] = s;
-}
-
-// G = sum over the partials, in a fixed order.
-__global__ void gram_reduce_kernel(const double* __restrict__ part, int n_parts, int D, double* __restrict__ G) {
+// G = sum over the partials of the CTAs in a fixed order, in fp64, with the
+// operand scale undone: the partials hold sums of (y * scale)(y * scale)^T.
+__global__ void gram_reduce_kernel(const double* __restrict__ part, int n_parts, int D,
+                                   const Meta* __restrict__ meta, double* __restrict__ G) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(D) * D) return;
   double s = 0.0;
   for (int p = 0; p < n_parts; ++p) s += part[static_cast<int64_t>(p) * D * D + e];
-  G[e] = s;
+  const double is = meta->inv_scale;
+  G[e] = s * is * is;
 }
 
 // Shared covariance of the M-step (one block per row d, thread e = column):
@@ -1608,10 +1532,7 @@ const void* kernel_handle(KernelId id) {
     case K_THRESH_SCAN: return reinterpret_cast<const void*>(&thresh_scan_kernel);
     case K_THRESH_SCATTER: return reinterpret_cast<const void*>(&thresh_scatter_kernel);
     case K_TIED_PREP: return reinterpret_cast<const void*>(&tied_prep_kernel);
-    case K_GRAM_BF16: return reinterpret_cast<const void*>(&gram_kernel<true>);
-    case K_GRAM_F32: return reinterpret_cast<const void*>(&gram_kernel<false>);
     case K_GRAM_REDUCE: return reinterpret_cast<const void*>(&gram_reduce_kernel);
-    case K_GRAM_REDUCE_F32: return reinterpret_cast<const void*>(&gram_reduce_f32_kernel);
     case K_SIGMA_TIED: return reinterpret_cast<const void*>(&sigma_tied_kernel);
     case K_BMAX: return reinterpret_cast<const void*>(&bmax_kernel);
   }

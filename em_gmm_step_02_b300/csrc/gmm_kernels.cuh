@@ -39,9 +39,17 @@ enum KernelId : int {
   K_FUSED_1_1_2, K_FUSED_1_2_2, K_FUSED_2_1_1, K_LSE_COMBINE, K_FINALIZE,
   K_TOPM_COMBINE, K_LL_TOTAL, K_TOPM_1_1_2, K_TOPM_1_2_2, K_TOPM_2_1_1,
   K_THRESH_COUNT, K_THRESH_SCAN, K_THRESH_SCATTER,
-  K_TIED_PREP, K_GRAM_BF16, K_GRAM_F32, K_GRAM_REDUCE, K_SIGMA_TIED, K_GRAM_REDUCE_F32,
+  K_TIED_PREP, K_GRAM_REDUCE, K_SIGMA_TIED,
   K_BMAX,
 };
+
+// The tied model's Gram matrix on the tensor cores (gram.cu): kernel handle for
+// np operand pieces, nch atom columns and bf16 or f32 data; its dynamic shared
+// memory and threads per CTA.  Launch: one CTA per SM (at most one per tile),
+// arguments (FusedArgs, double* partials [CTA][D][D]).
+const void* gram_handle(int np, int nch, bool xb);
+size_t gram_smem(int np, int nch);
+int gram_threads();
 
 // Handles of the two-team FAST kernels (em_fast.cu), nch = 1 or 2, one per
 // mode (MODE_EM, MODE_LSE, MODE_GIVEN, MODE_TOPM with candidate lists of
@@ -52,6 +60,17 @@ constexpr int kEmFastThreads = 512;
 
 // Threshold assignment: points per block of the count and scatter kernels.
 constexpr int kThreshBlock = 256;
+
+// Approximate top-k EM (topk_em.cu): points per tile of the counting sort
+// (one warp per tile), pairs per chunk of the statistics kernels, and the
+// kernels.  Launch shapes: COUNT and FILL one warp per tile (256 threads per
+// CTA); SCAN one CTA of 256 per component; BASE one CTA of 1024; STATS one
+// CTA of 128 per chunk (chunks beyond the device-side total return at once);
+// FINAL one CTA of 128 per component.
+constexpr int kTkTile = 4096;
+constexpr int kTkChunk = 2048;
+enum TopkKernel : int { TK_COUNT, TK_SCAN, TK_BASE, TK_FILL, TK_STATS1, TK_STATS2, TK_FINAL1, TK_FINAL2 };
+const void* topk_handle(TopkKernel id, bool xb);
 
 // Host-side handle of a kernel, for cudaLaunchKernelEx (argument order and
 // types as in gmm_kernels.cu).
@@ -92,6 +111,7 @@ struct FusedArgs {
   int32_t* topm_idx;      // MODE_TOPM output component indices, same layout
   int topm_groups;        // number of K groups (gridDim.y); 1: final output
   uint32_t* status;
+  uint32_t max_polls;     // polls per bounded wait (0: the default)
 };
 
 struct Small {
@@ -117,6 +137,7 @@ struct Small {
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
+  uint32_t poll_limit;     // follows abort_flag (read by the bounded waits)
 };
 
 // Shared-memory plan of the fused kernel for NP operand pieces (1: fp16,

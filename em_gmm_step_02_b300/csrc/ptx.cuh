@@ -122,14 +122,17 @@ __device__ __forceinline__ void note_timeout(const uint64_t* bar, uint32_t* stat
 
 // Polls allowed per wait before it is declared failed.  try_wait itself
 // suspends for a hardware-chosen interval, so this bounds the wait at a few
-// seconds at most.
+// seconds at most.  The kernels keep two adjacent shared words, the abort flag
+// and the poll limit of this launch (kMaxPolls unless the caller lowered it,
+// to exercise the failure path); `abort` points at the first.
 constexpr uint32_t kMaxPolls = 1u << 22;
 
 // Bounded wait for the phase with the given parity to complete.  Once any
 // wait in the kernel has failed (*abort set), later waits return at once.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort,
                                           uint32_t* status) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+  const uint32_t limit = abort[1];
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 63u && *abort) return false;
   }
@@ -153,7 +156,8 @@ __device__ __forceinline__ bool mbar_wait_final(uint64_t* bar, uint32_t parity, 
 
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
                                                   volatile uint32_t* abort, uint32_t* status) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+  const uint32_t limit = abort[1];
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((i & 63u) == 63u && *abort) return false;
   }

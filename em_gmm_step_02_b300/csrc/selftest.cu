@@ -28,7 +28,7 @@ selftest_mma_kernel(int variant, const uint4* __restrict__ a_img, const uint4* _
   uint8_t* sb = base + kOperandBytes;
   uint64_t* bar = reinterpret_cast<uint64_t*>(base + 2 * kOperandBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + 2 * kOperandBytes + 64);
-  __shared__ uint32_t abort_flag;
+  __shared__ uint32_t abort_flag[2];   // abort flag, poll limit
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool nosw = variant == 4;
@@ -42,7 +42,8 @@ selftest_mma_kernel(int variant, const uint4* __restrict__ a_img, const uint4* _
   for (int i = tid; i < b_bytes / 16; i += 128) reinterpret_cast<uint4*>(sb)[i] = b_img[i];
   fence_proxy_async_smem();
   if (tid == 0) {
-    abort_flag = 0;
+    abort_flag[0] = 0;
+    abort_flag[1] = kMaxPolls;
     mbar_init(bar, 1);
   }
   if (warp == 0) tmem_alloc(tmem_slot, 256);
@@ -71,7 +72,7 @@ selftest_mma_kernel(int variant, const uint4* __restrict__ a_img, const uint4* _
     mma_commit(bar);
   }
   __syncwarp();
-  mbar_wait(bar, 0, &abort_flag, status);
+  mbar_wait(bar, 0, abort_flag, status);
   tc_fence_after();
   const int row = warp * 32 + lane;
   for (int c = 0; c < N; c += 16) {

@@ -107,6 +107,13 @@ typedef struct {
     int32_t loglik_on_host;  /* 1: total_loglik is a host pointer; the call waits
                                 for the stream and reports device-side errors */
     int32_t plan;            /* gmm_plan_t, default AUTO */
+    int32_t wait_limit;      /* polls each device-side wait makes before it gives
+                                up and the call reports GMM_ERR_TIMEOUT; 0 (the
+                                default) = about 4 million (a few seconds).  Small
+                                values exist to test the failure path. */
+    int32_t approx_top_k;    /* gmm_em_step only: 0 (the default) or >= K = exact
+                                EM; 1 <= k < K: approximate top-k EM (see
+                                gmm_em_step) */
 } gmm_opts;
 
 /* Fill *opts with the defaults listed above. */
@@ -133,6 +140,18 @@ void gmm_default_opts(gmm_opts *opts);
  * Supported: 1 <= D <= 128, 1 <= K <= 8192 (K <= 1024 in a single pass over
  * X; above that the E-step's normaliser is computed in a first pass and kept
  * in an N-float buffer), N >= 1; PRECISE needs D <= 64.
+ *
+ * Approximate top-k EM (opts->approx_top_k = k, 1 <= k < K; the "GMMXX"
+ * README's training option approx_top_k): each point keeps its k largest
+ * logits l_ik and its responsibilities are normalised over those k only,
+ *   r_ik = exp(l_ik) / sum_{j kept} exp(l_ij)  (0 for the others),
+ * equal logits kept by the lower index first; the M-step above then runs
+ * with these responsibilities.  total_loglik stays the exact one (all K
+ * components).  The E-step is the top-m pass of gmm_predict_topm (m = k,
+ * same arithmetic); the statistics are gathered per component in point
+ * order (bit-identical on repeated calls), the variance in a second pass
+ * over the kept pairs.  Needs k <= 16, N < 2^31, SPHERICAL or DIAG, and a
+ * workspace of about 16 N k bytes more.
  */
 int gmm_em_step(const void *X, int64_t N, int32_t D, int32_t K, int32_t cov_type,
                 int32_t x_dtype, const float *log_weights, const float *means,
@@ -215,13 +234,14 @@ int gmm_em_step_host(const void *X_host, int64_t N, int32_t D, int32_t K, int32_
  * that must not call cudaMalloc/cudaFree because those calls can synchronise
  * the whole device.  The web pages describing the method have no counterpart
  * of this entry point.
- *  - Allocates nothing.  All scratch comes from one 40 MiB array compiled into
- *    this library; every GPU that loads the library keeps those 40 MiB
+ *  - Allocates nothing.  All scratch comes from one 24 MiB array compiled into
+ *    this library; every GPU that loads the library keeps those 24 MiB
  *    reserved until the process exits.  The caller passes inputs and outputs
  *    exactly as for gmm_em_step.
  *  - Limits: K <= 1024 (larger K needs an N-sized buffer) and the statistics
  *    of the problem must fit the array; when they fit only partly the step
- *    runs on fewer thread blocks.  Larger problems are rejected with
+ *    runs on fewer thread blocks (gmm_plan_info reports how many: at D = 128,
+ *    K = 1024 the array holds 11 of the 15 tile groups of a B300).  Larger problems are rejected with
  *    GMM_ERR_UNSUPPORTED and a message in gmm_last_error().
  *  - The first call with a given device current looks up the array's device
  *    address (cudaGetSymbolAddress) and sets kernel attributes; make that

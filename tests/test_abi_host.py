@@ -43,6 +43,19 @@ def test_argument_errors_are_found_on_the_host(kw, code):
     assert G.gmm_last_error() != ""
 
 
+def test_approx_top_k_argument_errors_are_found_on_the_host():
+    assert _call(K=40, opts=G.gmm_default_opts(approx_top_k=-1)) == -1
+    assert _call(K=40, opts=G.gmm_default_opts(approx_top_k=17)) == -2
+    assert _call(K=40, cov=2, D=8, opts=G.gmm_default_opts(approx_top_k=4)) == -2
+    assert "approx_top_k" in G.gmm_last_error()
+    assert _call(N=1 << 31, K=40, opts=G.gmm_default_opts(approx_top_k=4)) == -2
+    vp = ctypes.c_void_p
+    o = G.gmm_default_opts(approx_top_k=2)
+    assert G.lib().gmm_em_step_noalloc(vp(0x1000), 100, 8, 40, 1, 0, vp(0x2000), vp(0x2000), vp(0x2000),
+                                       vp(0x2000), vp(0x2000), vp(0x2000), vp(0x3000), ctypes.byref(o),
+                                       vp(0)) == -2
+
+
 def test_host_stream_argument_errors_are_found_on_the_host():
     vp = ctypes.c_void_p
     lib = G.lib()

@@ -1,17 +1,12 @@
-"""Parity of the CUDA EM step (through the C ABI) with the float64 oracle.
+"""Parity of the CUDA EM step (through the C ABI) with the float64 oracle,
+element by element (gpu_util.elementwise_errors states the denominators).
 
 Tolerances follow the method's stated accuracy targets:
-  PRECISE (float32 data): per-component relative L2 error of means, variances
-      and of the weight vector <= 1e-4; per-point mean log-likelihood within
-      1e-4 (absolute).
-  FAST (bf16 data): <= 2e-2 relative and 1e-2 (absolute) per-point mean
+  PRECISE (float32 data): weights, means and variances within 1e-4
+      relative; per-point mean log-likelihood within 1e-4 (absolute).
+  FAST (bf16 data): 2e-2 relative and 1e-2 (absolute) per-point mean
       log-likelihood; the log-likelihood after 20 iterations within 1e-3
       relative.
-Variances are compared on components holding at least MIN_NK effective
-points.  Below that a variance is a difference of two nearly equal moments of
-one or two points and carries no stable relative digits in either
-implementation; for those components the raw second moment (s2 + mu^2) is
-compared instead, with the same tolerance.
 """
 import numpy as np
 import pytest
@@ -20,10 +15,9 @@ import torch
 import em_gmm_step_02_b300 as G
 import oracle
 import workloads as W
-from gpu_util import params_to_device, rel_l2_rows
+from gpu_util import elementwise_errors, params_to_device, rel_l2_rows
 
 TOL = {"precise": (1e-4, 1e-4), "fast": (2e-2, 1e-2)}
-MIN_NK = 16.0
 
 
 def run_gpu(X_cpu, lw, mu, var, cov, precision="auto", **kw):
@@ -35,24 +29,12 @@ def run_gpu(X_cpu, lw, mu, var, cov, precision="auto", **kw):
     return [t.cpu().numpy() for t in out[:3]] + [float(out[3].item())]
 
 
-def compare(got, ref, N, cov, path):
+def compare(got, ref, N, cov, path, x_dtype, means_in):
     tol, tol_ll = TOL[path]
-    lw_g, mu_g, var_g, ll_g = got
-    lw_r, mu_r, var_r, ll_r = ref
-    K = len(lw_r)
-    e_w = np.linalg.norm(np.exp(lw_g) - np.exp(lw_r)) / np.linalg.norm(np.exp(lw_r))
-    e_mu = rel_l2_rows(mu_g, mu_r).max()
-    vg = np.asarray(var_g, np.float64).reshape(K, -1)
-    vr = np.asarray(var_r, np.float64).reshape(K, -1)
-    big = np.exp(lw_r) * N >= MIN_NK
-    e_var = rel_l2_rows(vg[big], vr[big]).max() if big.any() else 0.0
-    m2g = vg + (mu_g.astype(np.float64) ** 2 if cov == "diag" else (mu_g.astype(np.float64) ** 2).mean(1, keepdims=True))
-    m2r = vr + (mu_r ** 2 if cov == "diag" else (mu_r ** 2).mean(1, keepdims=True))
-    e_m2 = rel_l2_rows(m2g, m2r).max()
-    e_ll = abs(ll_g - ll_r) / N
-    msg = (f"w {e_w:.2e} mu {e_mu:.2e} var {e_var:.2e} ({big.sum()}/{K} comps) m2 {e_m2:.2e} "
-           f"ll/N {e_ll:.2e} (tol {tol}, {tol_ll})")
-    assert e_w <= tol and e_mu <= tol and e_var <= tol and e_m2 <= tol and e_ll <= tol_ll, msg
+    e_w, e_mu, e_v, msg = elementwise_errors(got[:3], ref, N, cov, path, tol, x_dtype, means_in)
+    e_ll = abs(got[3] - ref[3]) / N
+    msg += f" ll/N {e_ll:.2e} (tol {tol}, {tol_ll})"
+    assert e_w <= 1 and e_mu <= 1 and e_v <= 1 and e_ll <= tol_ll, msg
     return msg
 
 
@@ -63,7 +45,7 @@ def one_step_case(w, rows=None, precision="auto", path=None):
     got = run_gpu(X, *init, w.cov, precision)
     if path is None:
         path = "fast" if (precision == "fast" or (precision == "auto" and w.x_dtype == "bf16")) else "precise"
-    return compare(got, ref, X.shape[0], w.cov, path)
+    return compare(got, ref, X.shape[0], w.cov, path, w.x_dtype, init[1])
 
 
 # --------------------------------------------------------------------------- small shapes
@@ -109,7 +91,7 @@ def test_one_step_small_split_plan(N, D, K, cov, xd, prec):
     ref = oracle.em_step(X.float().numpy(), *init, w.cov)
     got = run_gpu(X, *init, w.cov, prec, plan="split")
     path = "fast" if xd == "bf16" else "precise"
-    print(compare(got, ref, X.shape[0], w.cov, path))
+    print(compare(got, ref, X.shape[0], w.cov, path, xd, init[1]))
 
 
 def _moments_ok(X, lw2, mu2, var2, reg=1e-6):
@@ -261,3 +243,23 @@ def test_conservation_of_moments_full_size_embed():
         assert G.gmm_stream_status() == 0, G.gmm_last_error()
         _moments_ok(X, lw2, mu2, var2)
         assert np.isfinite(ll.item())
+
+
+# --------------------------------------------------------------------------- flush periods
+@pytest.mark.gpu
+@pytest.mark.parametrize("N,D,K,cov,xd,path", [
+    (800_000, 8, 1024, "diag", "bf16", "fast"),
+    (500_000, 64, 256, "diag", "f32", "precise"),
+])
+def test_several_flush_periods_against_oracle(N, D, K, cov, xd, path):
+    """Every CTA accumulates at least three flush periods of statistics in
+    tensor memory before the fixed-order reduction (the periodic flush, not
+    only the one at the end of the CTA's tiles, is compared with the oracle)."""
+    info = G.gmm_plan_info(N, D, K, cov, xd, precision=path)
+    assert info["tiles"] // info["tile_groups"] >= 3 * info["flush_tiles"], info
+    w = W.generic(N, D, K, cov, xd, seed=N % 997 + K)
+    X = W.make_data(w)
+    init = W.make_init(w, X)
+    ref = oracle.em_step(X.float().numpy(), *init, cov)
+    got = run_gpu(X, *init, cov, path)
+    print(compare(got, ref, N, cov, path, xd, init[1]))

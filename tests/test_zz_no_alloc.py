@@ -68,3 +68,23 @@ def test_noalloc_rejects_large_k():
     with pytest.raises(G.GmmError) as e:
         G.gmm_em_step_noalloc(X, *p, "diag", out=out)
     assert e.value.code == -2
+
+
+@pytest.mark.gpu
+def test_noalloc_with_fewer_tile_groups_than_planned():
+    """At D = 128, K = 1024 the per-group statistics (2.1 MB each) fill the
+    fixed array before every co-resident cluster has a group, so the step runs
+    on fewer tile groups than gmm_em_step; the result must still agree."""
+    N, D, K = 60000, 128, 1024
+    info = G.gmm_plan_info(N, D, K, "diag", "bf16")
+    assert 0 < info["noalloc_tile_groups"] < info["tile_groups"], info
+    w = W.generic(N, D, K, "diag", "bf16", seed=13)
+    X = W.make_data(w).cuda()
+    p = params_to_device(*W.make_init(w, X.cpu()))
+    ref = G.gmm_em_step(X, *p, "diag")
+    torch.cuda.synchronize()
+    out = (torch.empty_like(p[0]), torch.empty_like(p[1]), torch.empty_like(p[2]),
+           torch.empty(1, dtype=torch.float64, device="cuda"))
+    G.gmm_em_step_noalloc(X, *p, "diag", out=out)
+    torch.cuda.synchronize()
+    _close(out, ref, N, 2e-2, 1e-2)
