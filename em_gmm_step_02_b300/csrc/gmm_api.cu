@@ -662,16 +662,21 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
 // pairs, the per-chunk partial statistics and N_k, then the top-m pass's
 // own space.
 struct TopkSpace {
-  int64_t T;            // tiles of kTkTile points
+  int tile;             // points per tile of the counting sort
+  int64_t T;            // tiles
   int64_t max_chunks;   // bound on the chunks of kTkChunk pairs over all components
-  size_t off_r, off_i, off_cnt, off_tot, off_base, off_cbase, off_pt, off_rw, off_part, off_nk;
+  size_t off_r, off_i, off_cnt, off_tot, off_base, off_cbase, off_pt, off_rw, off_part;
   TopmSpace tm;
   size_t end;
 };
 TopkSpace topk_space(const Plan& p, int k, size_t base) {
   TopkSpace t;
   const size_t nk = static_cast<size_t>(p.N) * k;
-  t.T = (p.N + kTkTile - 1) / kTkTile;
+  // 512 points per tile (short serial walks), doubled while the count table
+  // K x tiles would exceed 2^25 entries
+  t.tile = 512;
+  while (static_cast<int64_t>(p.K) * ((p.N + t.tile - 1) / t.tile) > (int64_t(1) << 25)) t.tile *= 2;
+  t.T = (p.N + t.tile - 1) / t.tile;
   t.max_chunks = static_cast<int64_t>(nk / kTkChunk) + p.K + 1;
   t.off_r = base;
   t.off_i = t.off_r + align256(sizeof(float) * nk);
@@ -682,8 +687,7 @@ TopkSpace topk_space(const Plan& p, int k, size_t base) {
   t.off_pt = t.off_cbase + align256(sizeof(int32_t) * (p.K + 1));
   t.off_rw = t.off_pt + align256(sizeof(uint32_t) * nk);
   t.off_part = t.off_rw + align256(sizeof(float) * nk);
-  t.off_nk = t.off_part + align256(sizeof(double) * static_cast<size_t>(t.max_chunks) * (p.D + 1));
-  t.tm = topm_space(p, k, t.off_nk + align256(sizeof(double) * p.K));
+  t.tm = topm_space(p, k, t.off_part + align256(sizeof(double) * static_cast<size_t>(t.max_chunks) * (3 * p.D + 1)));
   t.end = t.tm.end;
   return t;
 }
@@ -714,37 +718,27 @@ int run_topk_mstep(const Plan& p, const void* X, int k, const gmm_opts& o, uint8
   uint32_t* pt = reinterpret_cast<uint32_t*>(ws + t.off_pt);
   float* rw = reinterpret_cast<float*>(ws + t.off_rw);
   double* part = reinterpret_cast<double*>(ws + t.off_part);
-  double* nk = reinterpret_cast<double*>(ws + t.off_nk);
   const int32_t* idx = reinterpret_cast<const int32_t*>(ws + t.off_i);
   const float* resp = reinterpret_cast<const float*>(ws + t.off_r);
   const unsigned tile_blocks = static_cast<unsigned>((t.T + 7) / 8);
   const unsigned chunk_blocks = static_cast<unsigned>(t.max_chunks);
-  const int cov_diag = p.cov_diag;
   CUDA_TRY(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * static_cast<size_t>(p.K) * t.T, s));
-  if ((r = launch(topk_handle(TK_COUNT, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, p.N, k, p.K, t.T, cnt)))
+  if ((r = launch(topk_handle(TK_COUNT, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, p.N, k, p.K, t.T, t.tile,
+                  cnt)))
     return r;
   if ((r = launch(topk_handle(TK_SCAN, xb), dim3(p.K), dim3(256), 0, s, 1, cnt, t.T, tot))) return r;
   if ((r = launch(topk_handle(TK_BASE, xb), dim3(1), dim3(1024), 0, s, 1, static_cast<const int32_t*>(tot), p.K,
                   base, cbase)))
     return r;
-  if ((r = launch(topk_handle(TK_FILL, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, resp, p.N, k, p.K, t.T, cnt,
-                  static_cast<const int64_t*>(base), pt, rw)))
+  if ((r = launch(topk_handle(TK_FILL, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, resp, p.N, k, p.K, t.T,
+                  t.tile, cnt, static_cast<const int64_t*>(base), pt, rw)))
     return r;
-  const float* nm = new_means;
-  if ((r = launch(topk_handle(TK_STATS1, xb), dim3(chunk_blocks), dim3(128), 0, s, 1, X, p.D, p.K,
+  if ((r = launch(topk_handle(TK_STATS, xb), dim3(chunk_blocks), dim3(128), 0, s, 1, X, p.D, p.K,
                   static_cast<const int64_t*>(base), static_cast<const int32_t*>(cbase),
-                  static_cast<const uint32_t*>(pt), static_cast<const float*>(rw), nm, part)))
+                  static_cast<const uint32_t*>(pt), static_cast<const float*>(rw), part)))
     return r;
-  if ((r = launch(topk_handle(TK_FINAL1, xb), dim3(p.K), dim3(128), 0, s, 1, static_cast<const double*>(part),
-                  static_cast<const int32_t*>(cbase), p.N, p.D, cov_diag, o.reg_covar, o.var_floor, means, vars, nk,
-                  new_log_weights, new_means, new_vars)))
-    return r;
-  if ((r = launch(topk_handle(TK_STATS2, xb), dim3(chunk_blocks), dim3(128), 0, s, 1, X, p.D, p.K,
-                  static_cast<const int64_t*>(base), static_cast<const int32_t*>(cbase),
-                  static_cast<const uint32_t*>(pt), static_cast<const float*>(rw), nm, part)))
-    return r;
-  return launch(topk_handle(TK_FINAL2, xb), dim3(p.K), dim3(128), 0, s, 1, static_cast<const double*>(part),
-                static_cast<const int32_t*>(cbase), p.N, p.D, cov_diag, o.reg_covar, o.var_floor, means, vars, nk,
+  return launch(topk_handle(TK_FINAL, xb), dim3(p.K), dim3(128), 0, s, 1, static_cast<const double*>(part),
+                static_cast<const int32_t*>(cbase), p.N, p.D, p.cov_diag, o.reg_covar, o.var_floor, means, vars,
                 new_log_weights, new_means, new_vars);
 }
 

@@ -61,15 +61,14 @@ constexpr int kEmFastThreads = 512;
 // Threshold assignment: points per block of the count and scatter kernels.
 constexpr int kThreshBlock = 256;
 
-// Approximate top-k EM (topk_em.cu): points per tile of the counting sort
-// (one warp per tile), pairs per chunk of the statistics kernels, and the
-// kernels.  Launch shapes: COUNT and FILL one warp per tile (256 threads per
-// CTA); SCAN one CTA of 256 per component; BASE one CTA of 1024; STATS one
-// CTA of 128 per chunk (chunks beyond the device-side total return at once);
-// FINAL one CTA of 128 per component.
-constexpr int kTkTile = 4096;
+// Approximate top-k EM (topk_em.cu): pairs per chunk of the statistics
+// kernel and the kernels.  Launch shapes: COUNT and FILL one warp per tile of
+// points (256 threads per CTA); SCAN one CTA of 256 per component; BASE one
+// CTA of 1024; STATS one CTA of 128 per chunk (chunks beyond the device-side
+// total return at once; partials of 3 D + 1 doubles per chunk); FINAL one CTA
+// of 128 per component.
 constexpr int kTkChunk = 2048;
-enum TopkKernel : int { TK_COUNT, TK_SCAN, TK_BASE, TK_FILL, TK_STATS1, TK_STATS2, TK_FINAL1, TK_FINAL2 };
+enum TopkKernel : int { TK_COUNT, TK_SCAN, TK_BASE, TK_FILL, TK_STATS, TK_FINAL };
 const void* topk_handle(TopkKernel id, bool xb);
 
 // Host-side handle of a kernel, for cudaLaunchKernelEx (argument order and

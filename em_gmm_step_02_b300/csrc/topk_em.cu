@@ -11,9 +11,10 @@
 // sparse: point i adds to k components only.  They are gathered, not
 // scattered, so that every sum has one fixed order:
 //   1. tk_count:  a stable counting sort of the N k (point, component) pairs
-//                 by component.  Points are cut into tiles of kTkTile; one
-//                 warp walks one tile in point order and counts its pairs
-//                 per component (counts[c][t]).
+//                 by component.  Points are cut into tiles (512 points, more
+//                 when K times the number of tiles would pass 2^25); one warp
+//                 walks one tile in point order and counts its pairs per
+//                 component (counts[c][t]).
 //   2. tk_scan:   per component, the exclusive prefix over tiles; the total.
 //   3. tk_base:   the exclusive prefix over components (pair offsets) and the
 //                 chunking of every component's pairs into runs of kTkChunk.
@@ -21,11 +22,14 @@
 //                 (point, normalised responsibility) to its slot: within a
 //                 component, pairs are ordered by point index.
 //   5. tk_stats:  one CTA per chunk (a run of one component's pairs), one
-//                 thread per feature: pass 1 sums r and r x, pass 2 sums
-//                 r (x - mu')^2 with the new mean (the two-pass variance).
-//   6. tk_final:  one CTA per component sums its chunks in order (fp64) and
-//                 writes log pi, mu (pass 1) or the variance (pass 2), with the
-//                 floor, the regulariser and the empty-component rule.
+//                 thread per feature, one pass: sum r, sum r (x - s) and
+//                 sum r (x - s)^2 about a shift s inside the chunk (the row
+//                 of its largest responsibility).
+//   6. tk_final:  one CTA per component combines its chunks in order (fp64)
+//                 into N_k, the mean and the second moment about the mean
+//                 (the pairwise-combination form of the variance), then
+//                 writes log pi, mu and the variance with the floor, the
+//                 regulariser and the empty-component rule.
 // Every step reads the pairs and the data rows they name; nothing depends on
 // the order in which CTAs or warps run.
 #include <cuda_bf16.h>
@@ -56,12 +60,12 @@ __device__ __forceinline__ int pair_comp(const int32_t* __restrict__ idx, int64_
 // The warp owns column t alone, so plain read-modify-writes suffice; the
 // warp barrier orders them between steps.
 __global__ void __launch_bounds__(256) tk_count_kernel(const int32_t* __restrict__ idx, int64_t N, int k, int K,
-                                                       int64_t T, int32_t* __restrict__ counts) {
+                                                       int64_t T, int tile, int32_t* __restrict__ counts) {
   const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  const int64_t q0 = t * kTkTile * k;
-  const int64_t q1 = (t + 1) * kTkTile < N ? (t + 1) * kTkTile * k : N * k;
+  const int64_t q0 = t * tile * k;
+  const int64_t q1 = (t + 1) * tile < N ? (t + 1) * tile * k : N * k;
   for (int64_t b = q0; b < q1; b += 32) {
     const int c = pair_comp(idx, b + lane, q1, K);
     const unsigned grp = __match_any_sync(0xffffffffu, c);
@@ -147,14 +151,14 @@ __global__ void __launch_bounds__(1024) tk_base_kernel(const int32_t* __restrict
 // tile).  counts[c][t] (the exclusive prefix) is advanced as the cursor.
 // The responsibility is normalised over the point's k kept components.
 __global__ void __launch_bounds__(256) tk_fill_kernel(const int32_t* __restrict__ idx, const float* __restrict__ resp,
-                                                      int64_t N, int k, int K, int64_t T,
+                                                      int64_t N, int k, int K, int64_t T, int tile,
                                                       int32_t* __restrict__ counts, const int64_t* __restrict__ base,
                                                       uint32_t* __restrict__ pt, float* __restrict__ rw) {
   const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  const int64_t q0 = t * kTkTile * k;
-  const int64_t q1 = (t + 1) * kTkTile < N ? (t + 1) * kTkTile * k : N * k;
+  const int64_t q0 = t * tile * k;
+  const int64_t q1 = (t + 1) * tile < N ? (t + 1) * tile * k : N * k;
   for (int64_t b = q0; b < q1; b += 32) {
     const int64_t q = b + lane;
     const int c = pair_comp(idx, q, q1, K);
@@ -195,27 +199,66 @@ __device__ __forceinline__ float load_x(const void* X, int64_t off) {
   else return __ldg(reinterpret_cast<const float*>(X) + off);
 }
 
-// One CTA per chunk, thread d = feature d.  PASS 1: part[ch][d] = sum r x_d,
-// part[ch][D] = sum r.  PASS 2: part[ch][d] = sum r (x_d - mu'_d)^2.  Four
-// interleaved fp32 accumulators per thread (pair j goes to accumulator
+// One CTA per chunk, thread d = feature d, one pass over the chunk's pairs.
+// The sums are taken about a shift inside the chunk -- the data row of the
+// chunk's largest responsibility (the first such pair among equals) -- so that
+// the second moment about the final mean is formed without cancellation:
+//   part[ch] = [W, S1_0 .. S1_{D-1}, S2_0 .. S2_{D-1}, s_0 .. s_{D-1}],
+//   W = sum r, S1_d = sum r (x_d - s_d), S2_d = sum r (x_d - s_d)^2.
+// Four interleaved fp32 accumulators per thread (pair j goes to accumulator
 // j mod 4), added in a fixed order at the end.
-template <bool XB, int PASS>
+template <bool XB>
 __global__ void __launch_bounds__(128) tk_stats_kernel(const void* __restrict__ X, int D, int K,
                                                        const int64_t* __restrict__ base,
                                                        const int32_t* __restrict__ chunk_base,
                                                        const uint32_t* __restrict__ pt, const float* __restrict__ rw,
-                                                       const float* __restrict__ new_means,
                                                        double* __restrict__ part) {
+  __shared__ float s_best[4];
+  __shared__ int64_t s_pos[4];
   const int ch = blockIdx.x;
   if (ch >= chunk_base[K]) return;
   const int c = chunk_owner(chunk_base, K, ch);
   const int64_t q0 = base[c] + static_cast<int64_t>(ch - chunk_base[c]) * kTkChunk;
   const int64_t q1 = min(q0 + kTkChunk, base[c + 1]);
-  const int d = threadIdx.x;
+  const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
   const bool on = d < D;
-  const float mu = (PASS == 2 && on) ? new_means[static_cast<int64_t>(c) * D + d] : 0.f;
-  float a[4] = {0.f, 0.f, 0.f, 0.f};
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+
+  // the chunk's largest responsibility (lowest position among equals)
+  float best = -1.f;
+  int64_t bpos = q0;
+  for (int64_t q = q0 + d; q < q1; q += 128) {
+    const float r = __ldg(rw + q);
+    if (r > best) {
+      best = r;
+      bpos = q;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int64_t op = __shfl_xor_sync(0xffffffffu, bpos, o);
+    if (ob > best || (ob == best && op < bpos)) {
+      best = ob;
+      bpos = op;
+    }
+  }
+  if (lane == 0) {
+    s_best[warp] = best;
+    s_pos[warp] = bpos;
+  }
+  __syncthreads();
+  best = s_best[0];
+  bpos = s_pos[0];
+  for (int w = 1; w < 4; ++w)
+    if (s_best[w] > best || (s_best[w] == best && s_pos[w] < bpos)) {
+      best = s_best[w];
+      bpos = s_pos[w];
+    }
+  const float sh = on ? load_x<XB>(X, static_cast<int64_t>(__ldg(pt + bpos)) * D + d) : 0.f;
+
+  float a1[4] = {0.f, 0.f, 0.f, 0.f};
+  float a2[4] = {0.f, 0.f, 0.f, 0.f};
+  float w[4] = {0.f, 0.f, 0.f, 0.f};
   int64_t q = q0;
   for (; q + 8 <= q1; q += 8) {
     uint32_t i[8];
@@ -229,83 +272,86 @@ __global__ void __launch_bounds__(128) tk_stats_kernel(const void* __restrict__ 
     for (int j = 0; j < 8; ++j) x[j] = on ? load_x<XB>(X, static_cast<int64_t>(i[j]) * D + d) : 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      if constexpr (PASS == 1) {
-        a[j & 3] = fmaf(r[j], x[j], a[j & 3]);
-        s[j & 3] += r[j];
-      } else {
-        const float y = x[j] - mu;
-        a[j & 3] = fmaf(r[j] * y, y, a[j & 3]);
-      }
+      const float y = x[j] - sh;
+      const float ry = r[j] * y;
+      a1[j & 3] += ry;
+      a2[j & 3] = fmaf(ry, y, a2[j & 3]);
+      w[j & 3] += r[j];
     }
   }
   for (int j = 0; q < q1; ++q, ++j) {
     const uint32_t i = __ldg(pt + q);
     const float r = __ldg(rw + q);
-    const float x = on ? load_x<XB>(X, static_cast<int64_t>(i) * D + d) : 0.f;
-    if constexpr (PASS == 1) {
-      a[j & 3] = fmaf(r, x, a[j & 3]);
-      s[j & 3] += r;
-    } else {
-      const float y = x - mu;
-      a[j & 3] = fmaf(r * y, y, a[j & 3]);
-    }
+    const float y = (on ? load_x<XB>(X, static_cast<int64_t>(i) * D + d) : 0.f) - sh;
+    const float ry = r * y;
+    a1[j & 3] += ry;
+    a2[j & 3] = fmaf(ry, y, a2[j & 3]);
+    w[j & 3] += r;
   }
-  double* out = part + static_cast<int64_t>(ch) * (D + 1);
-  if (on) out[d] = (static_cast<double>(a[0]) + a[1]) + (static_cast<double>(a[2]) + a[3]);
-  if (PASS == 1 && d == 0) out[D] = (static_cast<double>(s[0]) + s[1]) + (static_cast<double>(s[2]) + s[3]);
+  double* out = part + static_cast<int64_t>(ch) * (3 * D + 1);
+  if (d == 0) out[0] = (static_cast<double>(w[0]) + w[1]) + (static_cast<double>(w[2]) + w[3]);
+  if (on) {
+    out[1 + d] = (static_cast<double>(a1[0]) + a1[1]) + (static_cast<double>(a1[2]) + a1[3]);
+    out[1 + D + d] = (static_cast<double>(a2[0]) + a2[1]) + (static_cast<double>(a2[2]) + a2[3]);
+    out[1 + 2 * D + d] = sh;
+  }
 }
 
-// One CTA per component, thread d = feature d: the component's chunk
-// partials summed in chunk order.
-//   PASS 1: N_k; log pi_k = log(N_k / N) (-inf and the old mean when
-//           N_k < 1e-30); mu'_kd = S1_kd / N_k.  N_k is kept in nk[c].
-//   PASS 2: s2 = S2 / N_k (diagonal), or sum_d S2_d / (D N_k) (spherical);
-//           new variance max(s2, var_floor) + reg_covar (the old one when
-//           N_k < 1e-30).
-template <int PASS>
+// One CTA per component, thread d = feature d: the component's chunks
+// combined in chunk order in fp64 (each chunk's sums are about its own shift
+// s_c):
+//   N_k  = sum_c W_c;  log pi_k = log(N_k / N);
+//   mu_d = sum_c (S1_cd + W_c s_cd) / N_k;
+//   M2_d = sum_c [S2_cd + 2 (s_cd - mu_d) S1_cd + W_c (s_cd - mu_d)^2]
+//        = sum_i r_i (x_id - mu_d)^2;
+//   variance M2_d / N_k (diagonal) or sum_d M2_d / (D N_k) (spherical), then
+//   max(., var_floor) + reg_covar.  N_k < 1e-30: log pi = -inf, mean and
+//   variance kept.
 __global__ void __launch_bounds__(128) tk_final_kernel(const double* __restrict__ part,
                                                        const int32_t* __restrict__ chunk_base, int64_t N, int D,
                                                        int cov_diag, float reg_covar, float var_floor,
-                                                       const float* means, const float* vars, double* __restrict__ nk,
+                                                       const float* means, const float* vars,
                                                        float* new_log_weights, float* new_means, float* new_vars) {
   __shared__ double red[128];
   const int c = blockIdx.x, d = threadIdx.x;
   const int ch0 = chunk_base[c], ch1 = chunk_base[c + 1];
-  double sd = 0.0, s0 = 0.0;
+  const int64_t stride = 3 * D + 1;
+  double W = 0.0, t1 = 0.0;
   for (int ch = ch0; ch < ch1; ++ch) {
-    const double* p = part + static_cast<int64_t>(ch) * (D + 1);
-    if (d < D) sd += p[d];
-    if (PASS == 1) s0 += p[D];
+    const double* p = part + ch * stride;
+    W += p[0];
+    if (d < D) t1 += p[1 + d] + p[0] * p[1 + 2 * D + d];
   }
   constexpr double kEmpty = 1e-30;
-  if constexpr (PASS == 1) {
-    const bool empty = !(s0 >= kEmpty);
-    if (d == 0) {
-      nk[c] = s0;
-      new_log_weights[c] = empty ? -INFINITY : static_cast<float>(log(s0 / static_cast<double>(N)));
+  const bool empty = !(W >= kEmpty);
+  const double mu = d < D ? t1 / W : 0.0;
+  double m2 = 0.0;
+  if (!empty && d < D) {
+    for (int ch = ch0; ch < ch1; ++ch) {
+      const double* p = part + ch * stride;
+      const double e = p[1 + 2 * D + d] - mu;
+      m2 += p[1 + D + d] + 2.0 * e * p[1 + d] + p[0] * e * e;
     }
+  }
+  if (d == 0) new_log_weights[c] = empty ? -INFINITY : static_cast<float>(log(W / static_cast<double>(N)));
+  if (d < D) {
+    const int64_t o = static_cast<int64_t>(c) * D + d;
+    new_means[o] = empty ? means[o] : static_cast<float>(mu);
+  }
+  if (cov_diag) {
     if (d < D) {
       const int64_t o = static_cast<int64_t>(c) * D + d;
-      new_means[o] = empty ? means[o] : static_cast<float>(sd / s0);
+      new_vars[o] = empty ? vars[o] : static_cast<float>(fmax(m2 / W, static_cast<double>(var_floor)) + reg_covar);
     }
   } else {
-    const double n = nk[c];
-    const bool empty = !(n >= kEmpty);
-    if (cov_diag) {
-      if (d < D) {
-        const int64_t o = static_cast<int64_t>(c) * D + d;
-        new_vars[o] = empty ? vars[o] : static_cast<float>(fmax(sd / n, static_cast<double>(var_floor)) + reg_covar);
-      }
-    } else {
-      red[d] = d < D ? sd : 0.0;
-      __syncthreads();
-      if (d == 0) {
-        double t = 0.0;
-        for (int e = 0; e < D; ++e) t += red[e];
-        new_vars[c] = empty ? vars[c]
-                            : static_cast<float>(fmax(t / (static_cast<double>(D) * n), static_cast<double>(var_floor)) +
-                                                 reg_covar);
-      }
+    red[d] = d < D ? m2 : 0.0;
+    __syncthreads();
+    if (d == 0) {
+      double t = 0.0;
+      for (int e = 0; e < D; ++e) t += red[e];
+      new_vars[c] = empty ? vars[c]
+                          : static_cast<float>(fmax(t / (static_cast<double>(D) * W), static_cast<double>(var_floor)) +
+                                               reg_covar);
     }
   }
 }
@@ -318,14 +364,10 @@ const void* topk_handle(TopkKernel id, bool xb) {
     case TK_SCAN: return reinterpret_cast<const void*>(&tk_scan_kernel);
     case TK_BASE: return reinterpret_cast<const void*>(&tk_base_kernel);
     case TK_FILL: return reinterpret_cast<const void*>(&tk_fill_kernel);
-    case TK_STATS1:
-      return xb ? reinterpret_cast<const void*>(&tk_stats_kernel<true, 1>)
-                : reinterpret_cast<const void*>(&tk_stats_kernel<false, 1>);
-    case TK_STATS2:
-      return xb ? reinterpret_cast<const void*>(&tk_stats_kernel<true, 2>)
-                : reinterpret_cast<const void*>(&tk_stats_kernel<false, 2>);
-    case TK_FINAL1: return reinterpret_cast<const void*>(&tk_final_kernel<1>);
-    case TK_FINAL2: return reinterpret_cast<const void*>(&tk_final_kernel<2>);
+    case TK_STATS:
+      return xb ? reinterpret_cast<const void*>(&tk_stats_kernel<true>)
+                : reinterpret_cast<const void*>(&tk_stats_kernel<false>);
+    case TK_FINAL: return reinterpret_cast<const void*>(&tk_final_kernel);
   }
   return nullptr;
 }
