@@ -168,6 +168,75 @@ __device__ __forceinline__ void team_loop(const FusedArgs& a, uint8_t* sm, FastS
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) Mc[c] = 0.f;
+    } else if constexpr (lse_only) {
+      // ---- this CTA's normaliser only: online max and sum over 32-column
+      // chunks, nothing kept for a responsibility tile
+      float M = -CUDART_INF_F;
+      float ssum = 0.f;                      // sum of 2^(l - M) (log2 units)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float w0[32], w1[32];
+        tmem_ld32(acc + lane_off + 64 * h, w0);
+        tmem_ld32(acc + lane_off + 64 * h + 32, w1);
+        tmem_wait_ld();
+        if (h == 1) {
+          tc_fence_before();
+          mbar_arrive(&S->acc_empty[t]);
+        }
+        float mq[4] = {w0[0], w0[1], w0[2], w0[3]};
+#pragma unroll
+        for (int e = 4; e < 32; e += 4) {
+          mq[0] = fmaxf(mq[0], w0[e]);
+          mq[1] = fmaxf(mq[1], w0[e + 1]);
+          mq[2] = fmaxf(mq[2], w0[e + 2]);
+          mq[3] = fmaxf(mq[3], w0[e + 3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          mq[0] = fmaxf(mq[0], w1[e]);
+          mq[1] = fmaxf(mq[1], w1[e + 1]);
+          mq[2] = fmaxf(mq[2], w1[e + 2]);
+          mq[3] = fmaxf(mq[3], w1[e + 3]);
+        }
+        const float Mn = fmaxf(M, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
+        if (Mn > M && M > -CUDART_INF_F) ssum *= ex2((M - Mn) * is);
+        M = Mn;
+        if (M > -CUDART_INF_F) {
+          const float off = -M * is;
+          float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            sq[e & 3] += ex2(fmaf(w0[e], is, off));
+            sq[(e + 2) & 3] += ex2(fmaf(w1[e], is, off));
+          }
+          ssum += (sq[0] + sq[1]) + (sq[2] + sq[3]);
+        }
+      }
+      lse = ssum > 0.f ? M * is + lg2(ssum) : -CUDART_INF_F;
+      if (exch) {
+        if (jj > 0) mbar_wait_cluster(&S->xfree[t], static_cast<uint32_t>((jj - 1) & 1), abort_flag, a.status);
+        const uint32_t dst = smem_u32(&S->xrecv[t][rank][nl]);
+        const uint32_t bar = smem_u32(&S->xready[t]);
+        for (int r = 0; r < C; ++r) st_async_f32(mapa(dst, r), lse, mapa(bar, r));
+        if (q == 0 && lane == 0) mbar_arrive_expect_tx(&S->xready[t], static_cast<uint32_t>(C * kBN * 4));
+        mbar_wait_cluster(&S->xready[t], static_cast<uint32_t>(jj & 1), abort_flag, a.status);
+        float vals[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) vals[r] = r < C ? S->xrecv[t][r][nl] : -CUDART_INF_F;
+        __syncwarp();
+        if (lane < C) mbar_arrive_remote_relaxed(mapa(smem_u32(&S->xfree[t]), static_cast<uint32_t>(lane)));
+        float mx = vals[0];
+#pragma unroll
+        for (int r = 1; r < 8; ++r) mx = fmaxf(mx, vals[r]);
+        float s2 = 0.f;
+        if (mx > -CUDART_INF_F) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) s2 += ex2(vals[r] - mx);
+        }
+        lse = s2 > 0.f ? mx + lg2(s2) : -CUDART_INF_F;
+      }
+      if (rank == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
+      continue;
     } else {
       // ---- local online softmax over this CTA's 128 components
       float M = -CUDART_INF_F;
@@ -252,10 +321,6 @@ __device__ __forceinline__ void team_loop(const FusedArgs& a, uint8_t* sm, FastS
           for (int r = 0; r < 8; ++r) s2 += ex2(vals[r] - mx);
         }
         lse = s2 > 0.f ? mx + lg2(s2) : -CUDART_INF_F;
-      }
-      if constexpr (lse_only) {
-        if (rank == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
-        continue;
       }
       if (ll_row && valid) llf += lse;
       // r * 2^10 = p * 2^(M_c * is - lse)
@@ -639,6 +704,8 @@ __device__ __forceinline__ void mma_loop(const FusedArgs& a, uint8_t* sm, FastSm
     for (int c = 0; c < 2 * (CF::kDp / kAtomElems); ++c)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
+        // K steps wholly inside the zero padding beyond D add nothing
+        if ((c % (CF::kDp / kAtomElems)) * kAtomElems + 16 * kk >= a.D) continue;
         const uint64_t ad = sdesc_sw128(stage + c * kChunkBytes + 32 * kk, 16, 1024);
         const uint64_t bd = sdesc_sw128(sP + c * kChunkBytes + 32 * kk, 16, 1024);
         mma_f16_ss(acc, ad, bd, idl, accf);
@@ -768,13 +835,22 @@ __global__ void __launch_bounds__(512, 1) em_fast_kernel(const FusedArgs a) {
   tc_fence_after();
   const uint32_t tmem = S->tmem_base;
 
+  // Register split of the 512 threads launched at 128 registers (65,536 in
+  // all): transform warpgroup 112, the two softmax teams kTeamRegs, the MMA /
+  // S0 warpgroup kRestRegs, with 128 (112 + 2 kTeamRegs + kRestRegs) <= 65,536,
+  // i.e. 2 kTeamRegs + kRestRegs <= 400.  Per mode the teams take what their
+  // loop needs and the rest goes to the MMA warpgroup (each choice is the one
+  // without spills under -Xptxas -v).
+  constexpr int kTeamRegs = MODE == MODE_EM ? 160 : MODE == MODE_GIVEN ? 136 : 144;
+  constexpr int kRestRegs = MODE == MODE_EM ? 72 : MODE == MODE_GIVEN ? 120 : 104;
+  static_assert(2 * kTeamRegs + kRestRegs <= 400, "register split exceeds the launch's registers");
   const int wg = warp >> 2;
   if (wg == 0) {
     regs_release<112>();
     if (a.x_bf16) transform_warps<CF, FastSmall, 1, NCH, 2, true, false>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
     else transform_warps<CF, FastSmall, 1, NCH, 2, false, false>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
   } else if (wg <= 2) {
-    regs_claim<160>();
+    regs_claim<kTeamRegs>();
     if constexpr (MODE == MODE_TOPM)
       topm_team_loop<CF, MAXM>(a, sm, S, abort_flag, wg - 1, warp, lane, rank, C, tgroup, n_tgroups, my_tiles, tmem,
                                kbase);
@@ -782,7 +858,7 @@ __global__ void __launch_bounds__(512, 1) em_fast_kernel(const FusedArgs a) {
       team_loop<CF, MODE>(a, sm, S, abort_flag, wg - 1, warp, lane, rank, C, tgroup, n_tgroups, my_tiles, tmem, kbase,
                           kvalid);
   } else {
-    regs_release<72>();
+    regs_release<kRestRegs>();
     if (warp == 12) {
       if (lane == 0) {
         const uint32_t pbytes = static_cast<uint32_t>(CF::kPieceBytes);
