@@ -36,9 +36,9 @@ import workloads as W  # noqa: E402
 METRIC = "EM iter/s and N·K·D/s at N=10M,D=128,K=1024 diag; % tensor-core peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # dram__bytes_read.sum + dram__bytes_write.sum of one fused-kernel launch on the
-# full 10M x 128 workload: 297.1 MB (288.9 read + 8.1 written) measured on its
-# first 1M rows, times 10
-TRAFFIC_EMBED_10M = 2.971e9
+# full 10M x 128 workload: 303.5 MB (296.2 read + 7.3 written) measured on its
+# first 1M rows, times 10 (traffic grows in proportion to the rows)
+TRAFFIC_EMBED_10M = 3.035e9
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")

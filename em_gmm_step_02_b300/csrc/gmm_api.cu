@@ -733,7 +733,9 @@ int run_topk_mstep(const Plan& p, const void* X, int k, const gmm_opts& o, uint8
   if ((r = launch(topk_handle(TK_FILL, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, resp, p.N, k, p.K, t.T,
                   t.tile, cnt, static_cast<const int64_t*>(base), pt, rw)))
     return r;
-  if ((r = launch(topk_handle(TK_STATS, xb), dim3(chunk_blocks), dim3(128), 0, s, 1, X, p.D, p.K,
+  // 16-byte row loads when a row is a whole number of 16-byte units
+  const bool vec = (p.D * (xb ? 2 : 4)) % 16 == 0;
+  if ((r = launch(topk_handle(vec ? TK_STATS_VEC : TK_STATS, xb), dim3(chunk_blocks), dim3(128), 0, s, 1, X, p.D, p.K,
                   static_cast<const int64_t*>(base), static_cast<const int32_t*>(cbase),
                   static_cast<const uint32_t*>(pt), static_cast<const float*>(rw), part)))
     return r;

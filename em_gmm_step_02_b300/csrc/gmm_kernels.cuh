@@ -64,11 +64,12 @@ constexpr int kThreshBlock = 256;
 // Approximate top-k EM (topk_em.cu): pairs per chunk of the statistics
 // kernel and the kernels.  Launch shapes: COUNT and FILL one warp per tile of
 // points (256 threads per CTA); SCAN one CTA of 256 per component; BASE one
-// CTA of 1024; STATS one CTA of 128 per chunk (chunks beyond the device-side
-// total return at once; partials of 3 D + 1 doubles per chunk); FINAL one CTA
-// of 128 per component.
+// CTA of 1024; STATS / STATS_VEC one CTA of 128 per chunk (chunks beyond the
+// device-side total return at once; partials of 3 D + 1 doubles per chunk;
+// STATS_VEC for rows of a multiple of 16 bytes); FINAL one CTA of 128 per
+// component.
 constexpr int kTkChunk = 2048;
-enum TopkKernel : int { TK_COUNT, TK_SCAN, TK_BASE, TK_FILL, TK_STATS, TK_FINAL };
+enum TopkKernel : int { TK_COUNT, TK_SCAN, TK_BASE, TK_FILL, TK_STATS, TK_STATS_VEC, TK_FINAL };
 const void* topk_handle(TopkKernel id, bool xb);
 
 // Host-side handle of a kernel, for cudaLaunchKernelEx (argument order and

@@ -297,6 +297,158 @@ __global__ void __launch_bounds__(128) tk_stats_kernel(const void* __restrict__ 
   }
 }
 
+// The same statistics with 16-byte loads, for rows whose size is a multiple
+// of 16 bytes (bf16: D % 8 == 0; float32: D % 4 == 0).  A row is read by
+// TPR = D / V threads of V features each; the CTA's 128 threads form
+// G = 128 / TPR row groups, and group g takes the chunk's pairs g, g + G,
+// g + 2G, ... in order.  The groups' sums are added in group order (fp64) at
+// the end, so every sum still has one fixed order.
+template <bool XB>
+__global__ void __launch_bounds__(128) tk_stats_vec_kernel(const void* __restrict__ X, int D, int K,
+                                                           const int64_t* __restrict__ base,
+                                                           const int32_t* __restrict__ chunk_base,
+                                                           const uint32_t* __restrict__ pt,
+                                                           const float* __restrict__ rw, double* __restrict__ part) {
+  constexpr int V = XB ? 8 : 4;              // features per 16-byte load
+  __shared__ float s_best[4];
+  __shared__ int64_t s_pos[4];
+  __shared__ float s_a1[128 * V];            // [group][feature]
+  __shared__ float s_a2[128 * V];
+  __shared__ float s_w[128];
+  const int ch = blockIdx.x;
+  if (ch >= chunk_base[K]) return;
+  const int c = chunk_owner(chunk_base, K, ch);
+  const int64_t q0 = base[c] + static_cast<int64_t>(ch - chunk_base[c]) * kTkChunk;
+  const int64_t q1 = min(q0 + kTkChunk, base[c + 1]);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int TPR = D / V;
+  const int G = 128 / TPR;
+  const int g = tid / TPR, u = tid % TPR;
+  const bool on = g < G;
+
+  // the chunk's largest responsibility (lowest position among equals)
+  float best = -1.f;
+  int64_t bpos = q0;
+  for (int64_t q = q0 + tid; q < q1; q += 128) {
+    const float r = __ldg(rw + q);
+    if (r > best) {
+      best = r;
+      bpos = q;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int64_t op = __shfl_xor_sync(0xffffffffu, bpos, o);
+    if (ob > best || (ob == best && op < bpos)) {
+      best = ob;
+      bpos = op;
+    }
+  }
+  if (lane == 0) {
+    s_best[warp] = best;
+    s_pos[warp] = bpos;
+  }
+  __syncthreads();
+  best = s_best[0];
+  bpos = s_pos[0];
+  for (int w = 1; w < 4; ++w)
+    if (s_best[w] > best || (s_best[w] == best && s_pos[w] < bpos)) {
+      best = s_best[w];
+      bpos = s_pos[w];
+    }
+
+  auto load_row = [&](uint32_t i, float* x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(X) +
+                                                         (static_cast<int64_t>(i) * D + u * V) * (XB ? 2 : 4)));
+    if constexpr (XB) {
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(w4[e] << 16);
+        x[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u);
+      }
+    } else {
+      x[0] = __uint_as_float(v.x);
+      x[1] = __uint_as_float(v.y);
+      x[2] = __uint_as_float(v.z);
+      x[3] = __uint_as_float(v.w);
+    }
+  };
+
+  float sh[V], a1[V], a2[V];
+  float w = 0.f;
+#pragma unroll
+  for (int e = 0; e < V; ++e) a1[e] = a2[e] = 0.f;
+  if (on) {
+    load_row(__ldg(pt + bpos), sh);
+    int64_t q = q0 + g;
+    for (; q + 3 * G < q1; q += 4 * G) {
+      uint32_t i[4];
+      float r[4];
+      float x[4][V];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        i[j] = __ldg(pt + q + j * G);
+        r[j] = __ldg(rw + q + j * G);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) load_row(i[j], x[j]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          const float y = x[j][e] - sh[e];
+          const float ry = r[j] * y;
+          a1[e] += ry;
+          a2[e] = fmaf(ry, y, a2[e]);
+        }
+        w += r[j];
+      }
+    }
+    for (; q < q1; q += G) {
+      float x[V];
+      const float r = __ldg(rw + q);
+      load_row(__ldg(pt + q), x);
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const float y = x[e] - sh[e];
+        const float ry = r * y;
+        a1[e] += ry;
+        a2[e] = fmaf(ry, y, a2[e]);
+      }
+      w += r;
+    }
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      s_a1[g * D + u * V + e] = a1[e];
+      s_a2[g * D + u * V + e] = a2[e];
+    }
+    if (u == 0) s_w[g] = w;
+  }
+  __syncthreads();
+  double* out = part + static_cast<int64_t>(ch) * (3 * D + 1);
+  if (tid == 0) {
+    double tw = 0.0;
+    for (int gg = 0; gg < G; ++gg) tw += s_w[gg];
+    out[0] = tw;
+  }
+  for (int d = tid; d < D; d += 128) {
+    double t1 = 0.0, t2 = 0.0;
+    for (int gg = 0; gg < G; ++gg) {
+      t1 += s_a1[gg * D + d];
+      t2 += s_a2[gg * D + d];
+    }
+    out[1 + d] = t1;
+    out[1 + D + d] = t2;
+  }
+  // the shift of feature d, from the thread that loaded it (group 0)
+  if (g == 0) {
+#pragma unroll
+    for (int e = 0; e < V; ++e) out[1 + 2 * D + u * V + e] = sh[e];
+  }
+}
+
 // One CTA per component, thread d = feature d: the component's chunks
 // combined in chunk order in fp64 (each chunk's sums are about its own shift
 // s_c):
@@ -367,6 +519,9 @@ const void* topk_handle(TopkKernel id, bool xb) {
     case TK_STATS:
       return xb ? reinterpret_cast<const void*>(&tk_stats_kernel<true>)
                 : reinterpret_cast<const void*>(&tk_stats_kernel<false>);
+    case TK_STATS_VEC:
+      return xb ? reinterpret_cast<const void*>(&tk_stats_vec_kernel<true>)
+                : reinterpret_cast<const void*>(&tk_stats_vec_kernel<false>);
     case TK_FINAL: return reinterpret_cast<const void*>(&tk_final_kernel);
   }
   return nullptr;
