@@ -101,6 +101,7 @@ size_t fused_smem(int np, int nch, int nst) {
   if (np == 1 && nch == 1 && nst == 2) b = cfg_smem<1, 1, 2>();
   else if (np == 1 && nch == 2 && nst == 2) b = cfg_smem<1, 2, 2>();
   else if (np == 2 && nch == 1 && nst == 1) b = cfg_smem<2, 1, 1>();
+  else if (np == 2 && nch == 2 && nst == 1) b = cfg_smem<2, 2, 1>();
   return std::max<size_t>(b, 120 * 1024);   // one CTA per SM: it owns all of tensor memory
 }
 
@@ -108,6 +109,7 @@ const void* fused_fn(int np, int nch, int nst, bool topm = false) {
   if (np == 1 && nch == 1 && nst == 2) return kernel_handle(topm ? K_TOPM_1_1_2 : K_FUSED_1_1_2);
   if (np == 1 && nch == 2 && nst == 2) return kernel_handle(topm ? K_TOPM_1_2_2 : K_FUSED_1_2_2);
   if (np == 2 && nch == 1 && nst == 1) return kernel_handle(topm ? K_TOPM_2_1_1 : K_FUSED_2_1_1);
+  if (np == 2 && nch == 2 && nst == 1) return kernel_handle(topm ? K_TOPM_2_2_1 : K_FUSED_2_2_1);
   return nullptr;
 }
 
@@ -172,7 +174,6 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.nch = D <= 64 ? 1 : 2;
   p.np = p.fast ? 1 : 2;
   p.nst = p.fast ? 2 : 1;
-  if (!p.fast && p.nch != 1) return fail(GMM_ERR_UNSUPPORTED, "PRECISE arithmetic supports D <= 64");
   p.n_slices = (K + kSlice - 1) / kSlice;
   const bool split = o.plan == GMM_PLAN_SPLIT;
   p.two_pass = split || p.n_slices > 8;

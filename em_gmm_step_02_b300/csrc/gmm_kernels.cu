@@ -740,6 +740,10 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       mbar_init(&S->xready[i], 1);
     }
     mbar_init(&S->p_full, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&S->pfull[i], 1);
+      mbar_init(&S->pempty[i], 1);
+    }
     mbar_init(&S->acc1_full, 1);
     mbar_init(&S->acc1_empty, 256);
     for (int q = 0; q < 4; ++q) {
@@ -1016,12 +1020,14 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
     // ================================================= MMA warp
     if (lane == 0) {
       const size_t pbytes = static_cast<size_t>(NP) * CF::kPieceBytes;
-      mbar_arrive_expect_tx(&S->p_full, static_cast<uint32_t>(pbytes));
       const uint8_t* src = a.p_img + static_cast<size_t>(slice) * pbytes;
-      for (size_t o = 0; o < pbytes; o += 16384)
-        bulk_g2s(sm + CF::kOffP + o, src + o, 16384, &S->p_full);
-      mbar_wait(&S->p_full, 0, abort_flag, a.status);
-      tc_fence_after();
+      if constexpr (!CF::kStreamP) {
+        mbar_arrive_expect_tx(&S->p_full, static_cast<uint32_t>(pbytes));
+        for (size_t o = 0; o < pbytes; o += 16384)
+          bulk_g2s(sm + CF::kOffP + o, src + o, 16384, &S->p_full);
+        mbar_wait(&S->p_full, 0, abort_flag, a.status);
+        tc_fence_after();
+      }
 
       const uint32_t id1 = idesc_f16(kAbType, 0, 0, 128, n1);
       const uint32_t id2 = idesc_f16(kAbType, 1, 1, 128, 2 * CF::kDp);
@@ -1030,21 +1036,67 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       bool fresh = true;   // next statistics MMA starts a new accumulation
       const int nst = kTopm ? 1 : NST;   // MODE_TOPM: stage 1 holds the lists
 
+      // Streamed parameter image (CF::kStreamP): every tile reads the slice's
+      // image as a sequence of 8 chunks of 16 KB, chunk i = (piece i & 1,
+      // column block i >> 1), through a ring of kPRing slots.  Sequence
+      // number L = 8 * tile + i; slot L % kPRing, phase (L / kPRing) & 1.  A
+      // slot is refilled once the MMAs of its previous chunk have completed
+      // (tcgen05.commit to pempty); copies run two chunks ahead.
+      const int n_chunks = CF::kStreamP ? 8 * my_tiles : 0;
+      int n_copied = 0;
+      auto issue_copy = [&](int L) {
+        if (*abort_flag) return;
+        const int s = L % CF::kPRing;
+        if (L >= CF::kPRing)
+          mbar_wait(&S->pempty[s], static_cast<uint32_t>((L / CF::kPRing - 1) & 1), abort_flag, a.status);
+        const int i = L & 7;
+        mbar_arrive_expect_tx(&S->pfull[s], static_cast<uint32_t>(kChunkBytes));
+        bulk_g2s(sm + CF::kOffP + s * kChunkBytes, src + (i & 1) * CF::kPieceBytes + (i >> 1) * kChunkBytes,
+                 kChunkBytes, &S->pfull[s]);
+        n_copied = L + 1;
+      };
+
       auto issue_g1 = [&](int jj) {
         const int s = jj % nst;
         const uint32_t stage = sA + s * CF::kStageBytes;
         uint32_t accf = 0;
+        if constexpr (CF::kStreamP) {
+          if (jj == 0) {
+            if (n_chunks > 0) issue_copy(0);
+            if (n_chunks > 1) issue_copy(1);
+          }
+          for (int i = 0; i < 8; ++i) {
+            const int L = 8 * jj + i;
+            const int ps = L % CF::kPRing;
+            mbar_wait(&S->pfull[ps], static_cast<uint32_t>((L / CF::kPRing) & 1), abort_flag, a.status);
+            tc_fence_after();
+            const uint32_t pslot = sP + ps * kChunkBytes;
+            const int c = i >> 1;                 // column block of [x | x^2]
+            const int n_pa = (i & 1) ? 1 : 2;     // parameter hi: data hi and lo; parameter lo: data hi
+            for (int pa = 0; pa < n_pa; ++pa)
 #pragma unroll
-        for (int pr = 0; pr < (NP == 1 ? 1 : 3); ++pr) {
-          const int pa = pr == 2 ? 1 : 0;      // data piece
-          const int pp = pr == 1 ? 1 : 0;      // parameter piece
-          for (int c = 0; c < 2 * NCH; ++c)
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sdesc_sw128(stage + pa * CF::kPieceBytes + c * kChunkBytes + 32 * kk, 16, 1024);
-              const uint64_t bd = sdesc_sw128(sP + pp * CF::kPieceBytes + c * kChunkBytes + 32 * kk, 16, 1024);
-              mma_f16_ss(acc1, ad, bd, id1, accf);
-              accf = 1;
-            }
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sdesc_sw128(stage + pa * CF::kPieceBytes + c * kChunkBytes + 32 * kk, 16, 1024);
+                const uint64_t bd = sdesc_sw128(pslot + 32 * kk, 16, 1024);
+                mma_f16_ss(acc1, ad, bd, id1, accf);
+                accf = 1;
+              }
+            mma_commit(&S->pempty[ps]);
+            if (L + 2 < n_chunks) issue_copy(L + 2);
+          }
+        } else {
+#pragma unroll
+          for (int pr = 0; pr < (NP == 1 ? 1 : 3); ++pr) {
+            const int pa = pr == 2 ? 1 : 0;      // data piece
+            const int pp = pr == 1 ? 1 : 0;      // parameter piece
+            for (int c = 0; c < 2 * NCH; ++c)
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sdesc_sw128(stage + pa * CF::kPieceBytes + c * kChunkBytes + 32 * kk, 16, 1024);
+                const uint64_t bd = sdesc_sw128(sP + pp * CF::kPieceBytes + c * kChunkBytes + 32 * kk, 16, 1024);
+                mma_f16_ss(acc1, ad, bd, id1, accf);
+                accf = 1;
+              }
+          }
         }
         mma_commit(&S->acc1_full);
       };
@@ -1127,7 +1179,14 @@ __global__ void __launch_bounds__(416, 1) fused_em_kernel(const FusedArgs a) {
       // every copy and tensor-core operation of this CTA completes before the
       // tensor memory and shared memory are released (bounded waits that do not
       // give up early after another wait has failed)
-      mbar_wait_final(&S->p_full, 0, a.status);
+      if constexpr (CF::kStreamP) {
+        // the copies still in flight after an early stop (at most the last
+        // kPRing issued; each was awaited before use otherwise)
+        for (int L = n_copied - CF::kPRing < 0 ? 0 : n_copied - CF::kPRing; L < n_copied; ++L)
+          mbar_wait_final(&S->pfull[L % CF::kPRing], static_cast<uint32_t>((L / CF::kPRing) & 1), a.status);
+      } else {
+        mbar_wait_final(&S->p_full, 0, a.status);
+      }
       mma_commit(&S->drain);
       mbar_wait_final(&S->drain, 0, a.status);
     }
@@ -1521,9 +1580,11 @@ const void* kernel_handle(KernelId id) {
     case K_FUSED_1_1_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 1, 2, false>);
     case K_FUSED_1_2_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 2, 2, false>);
     case K_FUSED_2_1_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 1, 1, false>);
+    case K_FUSED_2_2_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 2, 1, false>);
     case K_TOPM_1_1_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 1, 2, true>);
     case K_TOPM_1_2_2: return reinterpret_cast<const void*>(&fused_em_kernel<1, 2, 2, true>);
     case K_TOPM_2_1_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 1, 1, true>);
+    case K_TOPM_2_2_1: return reinterpret_cast<const void*>(&fused_em_kernel<2, 2, 1, true>);
     case K_LSE_COMBINE: return reinterpret_cast<const void*>(&lse_combine_kernel);
     case K_FINALIZE: return reinterpret_cast<const void*>(&finalize_kernel);
     case K_TOPM_COMBINE: return reinterpret_cast<const void*>(&topm_combine_kernel);

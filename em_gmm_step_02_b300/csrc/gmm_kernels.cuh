@@ -40,7 +40,7 @@ enum KernelId : int {
   K_TOPM_COMBINE, K_LL_TOTAL, K_TOPM_1_1_2, K_TOPM_1_2_2, K_TOPM_2_1_1,
   K_THRESH_COUNT, K_THRESH_SCAN, K_THRESH_SCATTER,
   K_TIED_PREP, K_GRAM_REDUCE, K_SIGMA_TIED,
-  K_BMAX,
+  K_BMAX, K_FUSED_2_2_1, K_TOPM_2_2_1,
 };
 
 // The tied model's Gram matrix on the tensor cores (gram.cu): kernel handle for
@@ -125,6 +125,8 @@ struct Small {
   uint64_t full_a[2];
   uint64_t empty_g[2][8];  // per stage: 16-row group g no longer read by the MMAs
   uint64_t p_full;
+  uint64_t pfull[3];       // streamed parameter image: ring slot filled
+  uint64_t pempty[3];      // streamed parameter image: ring slot read by its MMAs
   uint64_t acc1_full;
   uint64_t acc1_empty;
   uint64_t r_full[4];     // lane quarter q's rows written to R slot q & 1 (64 threads), one phase per tile
@@ -142,7 +144,7 @@ struct Small {
 
 // Shared-memory plan of the fused kernel for NP operand pieces (1: fp16,
 // 2: fp16 hi/lo), NCH 64-feature atom columns per data part, NST data stages:
-//   [data stages | parameter image | Small | R tile | ones]
+//   [data stages | parameter image (or its ring) | Small | R tile | ones]
 // MODE_TOPM runs with one data stage; the second stage (or, with a single
 // stage, the R tile area) holds the per-row candidate lists.
 template <int NP, int NCH, int NST>
@@ -151,7 +153,13 @@ struct Cfg {
   static constexpr int kStageBytes = NP * kPieceBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffP = NST * kStageBytes;
-  static constexpr int kOffSmall = kOffP + NP * kPieceBytes;
+  // Two pieces of 128 features (PRECISE, D > 64): the 128 KB parameter image
+  // does not fit beside the 128 KB data stage, so it streams through a ring
+  // of kPRing 16 KB chunks, read again (from L2) for every tile.
+  static constexpr bool kStreamP = NP == 2 && NCH == 2;
+  static constexpr int kPRing = 3;
+  static constexpr int kParamBytes = kStreamP ? kPRing * kChunkBytes : NP * kPieceBytes;
+  static constexpr int kOffSmall = kOffP + kParamBytes;
   static constexpr int kOffR = (kOffSmall + static_cast<int>(sizeof(Small)) + 1023) / 1024 * 1024;
   static constexpr int kRBytes = 2 * kRSlotBytes * 2;                // 2 slots x 32 points x 128 comps x 16 bit
   static constexpr int kOffOnes = kOffR + NP * kRBytes;             // 16 x 64 fp16 ones

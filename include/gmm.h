@@ -139,7 +139,9 @@ void gmm_default_opts(gmm_opts *opts);
  * repeated calls give bit-identical results.
  * Supported: 1 <= D <= 128, 1 <= K <= 8192 (K <= 1024 in a single pass over
  * X; above that the E-step's normaliser is computed in a first pass and kept
- * in an N-float buffer), N >= 1; PRECISE needs D <= 64.
+ * in an N-float buffer), N >= 1.  PRECISE at D > 64 reads the parameter
+ * image again for every 128-point tile (it does not fit on chip beside the
+ * data); it is slower per element than at D <= 64.
  *
  * Approximate top-k EM (opts->approx_top_k = k, 1 <= k < K; the "GMMXX"
  * README's training option approx_top_k): each point keeps its k largest

@@ -117,3 +117,38 @@ def elementwise_errors(got, ref, N, cov, path, tol, x_dtype="bf16", means_in=Non
            f"(worst k={worst[0]}: ref {v_r[worst]:.3e} got {v_g[worst]:.3e} m2 {m2_r[worst]:.3e}); "
            f"small comps var {e_small.max():.2e}x bound")
     return e_w.max(), e_mu.max(), max(e_v.max(), e_small.max()), msg
+
+
+# ------------------------------------------------------------------ top-m bounds of PRECISE
+def precise_resp_tol(X, means, vars_, cov, idx, r, tol, tol_ll):
+    """Per-entry bound (N x m) on a PRECISE responsibility, the larger of tol
+    and 2 eps T min(r, 1 - r), and the bound on the per-point mean
+    log-likelihood, the larger of tol_ll and the mean of eps T (a row's
+    log-sum-exp moves by at most its largest logit error).  PRECISE resolves a
+    logit to about eps (natural-log units) of the size T of its expanded-form
+    terms: eps = (2^-22 + 2^-24 sqrt(n)) ln 2, the 22-bit operand pieces plus
+    the fp32 accumulation over the n = 3 * 2 D_pad / 16 MMA K steps of the
+    three products (rounding errors of a random walk),
+        T = sum_d ((x - s)^2 + 2 |x - s| |mu - s| + (mu - s)^2) / (2 s2)  (log2 units),
+    s the mean of the component means; T is taken as the largest over the
+    point's listed components.  A responsibility moves by
+    r_k (dl_k - sum_j r_j dl_j), at most 2 eps T r_k, and the largest one
+    by at most 2 eps T (1 - r_k) since the responsibilities sum to one."""
+    X = np.asarray(X, np.float64)
+    mu = np.asarray(means, np.float64)
+    K, D = mu.shape
+    v = np.asarray(vars_, np.float64)
+    v = np.repeat(v.reshape(K, 1), D, 1) if cov == "spherical" else v.reshape(K, D)
+    s = mu.mean(0)
+    y = X - s
+    ay = np.abs(y)
+    T = np.zeros(X.shape[0])
+    for j in range(idx.shape[1]):
+        k = np.asarray(idx[:, j])
+        nu = mu[k] - s
+        t = ((y * y + 2 * ay * np.abs(nu) + nu * nu) / (2 * v[k])).sum(1) * np.log2(np.e)
+        T = np.maximum(T, t)
+    d_pad = 64 * ((D + 63) // 64)
+    eps = (2.0 ** -22 + 2.0 ** -24 * np.sqrt(3 * 2 * d_pad / 16)) * np.log(2.0)
+    r = np.asarray(r, np.float64)
+    return np.maximum(tol, 2 * eps * T[:, None] * np.minimum(r, 1 - r)), max(tol_ll, float((eps * T).mean()))

@@ -36,7 +36,7 @@ def _call(N=100, D=8, K=4, cov=1, dt=0, X=0x1000, p=0x2000, ll=0x3000, opts=None
 @pytest.mark.parametrize("kw,code", [
     (dict(N=0), -1), (dict(D=0), -1), (dict(K=0), -1), (dict(cov=3), -1), (dict(dt=3), -1),
     (dict(X=0), -1), (dict(X=0x1004), -1), (dict(p=0x2002), -1), (dict(ll=0), -1),
-    (dict(D=129), -2), (dict(K=8193), -2), (dict(D=65, dt=0), -2),
+    (dict(D=129), -2), (dict(K=8193), -2),
 ])
 def test_argument_errors_are_found_on_the_host(kw, code):
     assert _call(**kw) == code

@@ -62,6 +62,11 @@ CASES = [
     (2500, 100, 300, "diag", "f32", "fast"),
     (12000, 32, 1100, "diag", "bf16", "auto"),
     (129, 5, 7, "spherical", "bf16", "auto"),
+    # float32 data with D > 64: PRECISE with the parameter image streamed per tile
+    (3001, 128, 256, "diag", "f32", "auto"),
+    (2500, 100, 300, "diag", "f32", "auto"),
+    (4000, 96, 129, "spherical", "f32", "auto"),
+    (6000, 128, 1100, "diag", "f32", "auto"),
 ]
 
 
@@ -155,15 +160,15 @@ def test_tiny_workload_20_iterations():
 
 # --------------------------------------------------------------------------- workload prefixes
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,rows", [
-    ("spherical_1m", 20000),
-    ("embed_10m", 20000),
-    ("descriptor_100m", 20000),
-    ("largek_2m", 30000),
+@pytest.mark.parametrize("name,rows,prec", [
+    ("spherical_1m", 20000, "auto"),
+    ("embed_10m", 20000, "auto"),
+    ("descriptor_100m", 20000, "auto"),    # float32, D = 128: PRECISE
+    ("descriptor_100m", 20000, "fast"),
+    ("largek_2m", 30000, "auto"),
 ])
-def test_workload_prefix_one_step(name, rows):
+def test_workload_prefix_one_step(name, rows, prec):
     w = W.WORKLOADS[name]
-    prec = "fast" if name == "descriptor_100m" else "auto"
     print(one_step_case(w.scaled(rows), precision=prec))
 
 
@@ -250,6 +255,7 @@ def test_conservation_of_moments_full_size_embed():
 @pytest.mark.parametrize("N,D,K,cov,xd,path", [
     (800_000, 8, 1024, "diag", "bf16", "fast"),
     (500_000, 64, 256, "diag", "f32", "precise"),
+    (500_000, 128, 256, "diag", "f32", "precise"),
 ])
 def test_several_flush_periods_against_oracle(N, D, K, cov, xd, path):
     """Every CTA accumulates at least three flush periods of statistics in

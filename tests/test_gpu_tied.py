@@ -32,6 +32,7 @@ def _case(N, D, K, xd, seed):
     (4000, 32, 16, "bf16", "precise"),   # bf16 data shifted by the mean of the means
     (20000, 128, 1024, "bf16", "auto"),  # clusters of 8 slices
     (12000, 32, 1100, "bf16", "auto"),   # two passes
+    (3000, 128, 16, "f32", "auto"),      # PRECISE, 128 features
 ])
 def test_tied_em_step_against_oracle(N, D, K, xd, prec):
     """Element by element: weights relative; means relative to the larger of
