@@ -53,8 +53,11 @@ struct Plan {
   int n_tiles;
   bool two_pass;
   int C;              // cluster size of the single pass
-  int C1;             // cluster size of pass 1 (two-pass): 8, or 1 in the SPLIT plan
-  int n_kgroups;      // pass 1 K groups (two-pass)
+  int C1;             // cluster size of the top-m pass (two-pass): 8, or 1 in the SPLIT plan
+  int n_kgroups;      // K groups of the top-m pass (two-pass)
+  int C1e;            // cluster size of the EM step's normaliser pass (two-pass)
+  int n_kgroups_e;    // K groups of the EM step's normaliser pass
+  int tg1e;           // tile groups of the EM step's normaliser pass
   int tg;             // tile groups of the statistics pass
   int tg1;            // tile groups of pass 1 (two-pass)
   int F;
@@ -194,6 +197,9 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
     int mc = need_device ? max_clusters(fn, p.smem, p.C, p.threads) : std::max(1, sms / p.C);
     p.tg = std::max(1, std::min(p.n_tiles, mc));
     p.tg1 = 0;
+    p.C1e = p.C;
+    p.n_kgroups_e = 1;
+    p.tg1e = 0;
   } else {
     p.C = p.C1;
     p.n_kgroups = p.n_slices / p.C1;
@@ -201,7 +207,30 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
     // every K group gets as many tile groups as clusters can be resident at
     // once; the groups run one after another in waves, each keeping the GPU full
     p.tg1 = std::max(1, std::min(p.n_tiles, mc));
-    p.tg = std::max(1, std::min(p.n_tiles, sms / p.n_slices));
+    // The EM step's normaliser pass runs without clusters (one normaliser per
+    // slice, no cross-CTA waits, every SM) when the per-slice normalisers fit
+    // in 4 GiB; the top-m pass keeps its groups of 8 (its candidate lists grow
+    // with the number of K groups).
+    const bool split_e = split || (o.plan == GMM_PLAN_AUTO &&
+                                   static_cast<double>(N) * p.n_slices * sizeof(float) <= 4.0 * (1 << 30));
+    p.C1e = split_e ? 1 : p.C1;
+    p.n_kgroups_e = p.n_slices / p.C1e;
+    p.tg1e = p.C1e == p.C1 ? p.tg1 : std::max(1, std::min(p.n_tiles, sms));
+    // statistics pass: n_slices x tg CTAs, one per SM at a time.  tg is chosen
+    // so that the waves come out nearly full (cost = waves x tiles per CTA),
+    // with the partial statistics (tg x K_pad x F doubles) at most 256 MiB.
+    int best = std::max(1, std::min(p.n_tiles, sms / p.n_slices));
+    int64_t best_cost = int64_t(1) << 62;
+    for (int tg = 1; tg <= std::min(p.n_tiles, 64); ++tg) {
+      if (static_cast<double>(tg) * p.K_pad * p.F * sizeof(double) > 256.0 * (1 << 20)) break;
+      const int64_t waves = (static_cast<int64_t>(p.n_slices) * tg + sms - 1) / sms;
+      const int64_t cost = waves * ((p.n_tiles + tg - 1) / tg);
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = tg;
+      }
+    }
+    p.tg = best;
   }
   // workspace layout
   size_t off = kStatusBytes;
@@ -218,7 +247,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.off_lsepart = off;
   p.off_lse = off;
   if (p.two_pass) {
-    off += align256(sizeof(float) * static_cast<size_t>(p.n_kgroups) * N);
+    off += align256(sizeof(float) * static_cast<size_t>(std::max(p.n_kgroups, p.n_kgroups_e)) * N);
     p.off_lse = off;
     off += align256(sizeof(float) * static_cast<size_t>(N));
   }
@@ -488,11 +517,13 @@ int run_estep(const Plan& p, const FusedArgs& a, uint8_t* ws, double* ll_part, c
     // pass 1: per-point normaliser over each group of 1024 components
     FusedArgs a1 = a;
     a1.mode = MODE_LSE;
-    a1.C = p.C1;
-    if ((r = launch_main(estep_fn(p, MODE_LSE), dim3(p.C1 * p.tg1, p.n_kgroups), dim3(p.threads), p.smem, s, p.C1, a1))) return r;
+    a1.C = p.C1e;
+    if ((r = launch_main(estep_fn(p, MODE_LSE), dim3(p.C1e * p.tg1e, p.n_kgroups_e), dim3(p.threads), p.smem, s,
+                         p.C1e, a1)))
+      return r;
     float* lse = reinterpret_cast<float*>(ws + p.off_lse);
     if ((r = launch(kernel_handle(K_LSE_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
-                    static_cast<const float*>(a.lse_part), p.n_kgroups, p.N, lse, ll_part)))
+                    static_cast<const float*>(a.lse_part), p.n_kgroups_e, p.N, lse, ll_part)))
       return r;
     *n_ll = kCombineBlocks;
     // pass 2: statistics of every slice given the normaliser
@@ -1218,10 +1249,10 @@ extern "C" int gmm_plan_info(int64_t N, int32_t D, int32_t K, int32_t cov_type, 
   Plan p;
   int r;
   if ((r = make_plan(p, nullptr, N, D, K, cov_type, x_dtype, o, true))) return r;
-  info[0] = p.two_pass ? p.C1 : p.C;
+  info[0] = p.two_pass ? p.C1e : p.C;
   info[1] = p.tg;
   info[2] = p.two_pass ? 1 : 0;
-  info[3] = p.two_pass ? p.tg1 : 0;
+  info[3] = p.two_pass ? p.tg1e : 0;
   info[4] = p.flush;
   info[5] = p.threads;
   info[6] = 0;

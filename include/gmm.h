@@ -96,7 +96,10 @@ typedef enum {
  *           and accumulates the statistics with the normaliser read from
  *           memory.  1.5 times the tensor-core work, no cross-CTA waits,
  *           N * ceil(K / 128) + N extra floats of workspace.
- *  AUTO:    the faster of the two for the shape (see gmm_em_step). */
+ *  AUTO:    CLUSTER for K <= 1024.  Above that the EM step takes two passes
+ *           either way, and AUTO runs its normaliser pass as in SPLIT (no
+ *           clusters) when the N x ceil(K / 128) normalisers fit in 4 GiB,
+ *           else in clusters of 8; the top-m pass keeps clusters of 8. */
 typedef enum { GMM_PLAN_AUTO = 0, GMM_PLAN_CLUSTER = 1, GMM_PLAN_SPLIT = 2 } gmm_plan_t;
 
 typedef struct {
@@ -282,7 +285,8 @@ void gmm_release(void);
 
 /* Launch plan of an EM step with these arguments on the current device (for
  * measurement and tests; no work is enqueued).  Fills info[0..7]:
- *   [0] CTAs per thread-block cluster (component slices sharing a point tile)
+ *   [0] CTAs per thread-block cluster (component slices sharing a point tile;
+ *       two-pass plan: of the EM step's normaliser pass)
  *   [1] tile groups of the statistics pass (co-resident clusters, or CTAs per
  *       slice in the two-pass plan)
  *   [2] 1 when the step takes two passes (K > 1024, or plan SPLIT)
