@@ -110,3 +110,20 @@ def test_workspace_is_independent_of_N_and_far_below_naive_footprint():
     b = G.gmm_workspace_bytes(100_000_000, 128, 1024, "diag", "bf16")
     assert a == b > 0
     assert b < 10_000_000 * 1024 * 4 / 100      # < 1% of the N x K matrix at N = 10M
+
+
+def test_plan_choices_for_large_k():
+    """K > 1024 takes two passes; with the AUTO plan the EM step's normaliser
+    pass runs without clusters while its N x slices normalisers fit in 4 GiB,
+    in clusters of 8 beyond that or when CLUSTER is asked for; the statistics
+    pass's tile groups keep the partials within 256 MiB."""
+    small = G.gmm_plan_info(2_000_000, 96, 8192, "diag", "bf16")
+    assert small["two_pass"] == 1 and small["cluster"] == 1
+    big = G.gmm_plan_info(20_000_000, 96, 8192, "diag", "bf16")
+    assert big["two_pass"] == 1 and big["cluster"] == 8
+    forced = G.gmm_plan_info(2_000_000, 96, 8192, "diag", "bf16", plan="cluster")
+    assert forced["cluster"] == 8
+    for info, K, F in ((small, 8192, 257), (big, 8192, 257)):
+        assert 1 <= info["tile_groups"] and info["tile_groups"] * K * F * 8 <= 256 << 20
+    one = G.gmm_plan_info(10_000_000, 128, 1024, "diag", "bf16")
+    assert one["two_pass"] == 0 and one["cluster"] == 8
