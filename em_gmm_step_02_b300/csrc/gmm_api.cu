@@ -255,7 +255,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.off_tl = p.off_sinv = p.off_twork = p.off_logdet = p.off_gram = p.off_gpart = p.off_tstats = p.off_tsig = off;
   if (p.cov_diag == GMM_TIED) {
     const size_t dd = sizeof(double) * static_cast<size_t>(D) * D;
-    p.n_gram = std::max(1, std::min(p.n_tiles, sms));   // one partial per CTA of the Gram kernel
+    p.n_gram = std::max(1, std::min(p.n_tiles, 2 * sms));   // one partial per CTA of the Gram kernel (two per SM)
     p.off_tl = off; off += align256(dd);
     p.off_sinv = off; off += align256(dd);
     p.off_twork = off; off += align256(dd);
@@ -403,12 +403,17 @@ int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, con
   double* logdet = tied ? reinterpret_cast<double*>(ws + p.off_logdet) : nullptr;
   if (tied) {
     // Sigma^-1 and log|Sigma| (one block), then the Gram matrix of the data
-    int r = launch(kernel_handle(K_TIED_PREP), dim3(1), dim3(128), 0, s, 1, var, p.D,
-                   reinterpret_cast<double*>(ws + p.off_tl), sinv, logdet,
-                   reinterpret_cast<double*>(ws + p.off_twork), status);
+    const size_t lbytes = sizeof(double) * static_cast<size_t>(p.D) * p.D;
+    int r = set_smem_attr(kernel_handle(K_TIED_PREP), lbytes);
+    if (r) return r;
+    r = launch(kernel_handle(K_TIED_PREP), dim3(1), dim3(128), lbytes, s, 1, var, p.D,
+               reinterpret_cast<double*>(ws + p.off_tl), logdet, status);
+    if (r) return r;
+    r = launch(kernel_handle(K_TIED_INV), dim3(p.D), dim3(128), 0, s, 1,
+               static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_tl)), p.D, sinv);
     if (r) return r;
     if (X) {
-      // G = sum (x - shift)(x - shift)^T on the tensor cores: one CTA per SM,
+      // G = sum (x - shift)(x - shift)^T on the tensor cores: two CTAs per SM,
       // fp64 partials per CTA, fixed-order reduction
       const void* gfn = gram_handle(p.np, p.nch, p.x_bf16 != 0);
       const size_t gsm = gram_smem(p.np, p.nch);
@@ -455,7 +460,7 @@ int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, con
 int run_tied_tail(const Plan& p, int K_stats, const gmm_opts& o, uint8_t* ws, float* new_vars, double* ll_dev,
                   cudaStream_t s) {
   float* out = new_vars ? new_vars : reinterpret_cast<float*>(ws + p.off_tsig);
-  return launch(kernel_handle(K_SIGMA_TIED), dim3(p.D), dim3(128), 0, s, 1,
+  return launch(kernel_handle(K_SIGMA_TIED), dim3((p.D + 15) / 16, (p.D + 15) / 16), dim3(256), 0, s, 1,
                 static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_gram)),
                 static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_tstats)), K_stats, p.D, p.N,
                 o.reg_covar, o.var_floor, static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_sinv)),

@@ -1383,13 +1383,14 @@ __global__ void finalize_kernel(const double* __restrict__ part, int n_parts, in
 // responsibilities of a point sum to one; the dropped per-point term of the
 // logits returns to the log-likelihood as -1/2 tr(Sigma^-1 G).
 
-// One block of D threads, fp64 in global scratch: the Cholesky factor L of
-// Sigma (row-major, lower), log|Sigma|, and Sigma^-1 (thread j solves
-// L y = e_j, L^T x = y for column j).  A matrix that is not positive definite
-// (or not finite) raises ST_NONFINITE.
-__global__ void tied_prep_kernel(const float* __restrict__ sigma, int D, double* __restrict__ L,
-                                 double* __restrict__ sinv, double* __restrict__ logdet,
-                                 double* __restrict__ work, uint32_t* __restrict__ status) {
+// One block of 128 threads with the Cholesky factor L of Sigma in shared
+// memory (fp64, row-major, lower; D * D * 8 bytes of dynamic shared memory):
+// L (written to global memory, zero above the diagonal) and log|Sigma|.  A
+// matrix that is not positive definite (or not finite) raises ST_NONFINITE.
+__global__ void __launch_bounds__(128) tied_prep_kernel(const float* __restrict__ sigma, int D,
+                                                        double* __restrict__ L, double* __restrict__ logdet,
+                                                        uint32_t* __restrict__ status) {
+  extern __shared__ double Ls[];
   const int t = threadIdx.x;
   __shared__ int bad;
   if (t == 0) bad = 0;
@@ -1397,45 +1398,72 @@ __global__ void tied_prep_kernel(const float* __restrict__ sigma, int D, double*
   for (int i = t; i < D * D; i += blockDim.x) {
     const float v = sigma[i];
     if (!isfinite(v)) bad = 1;
-    L[i] = v;
+    Ls[i] = v;
   }
   __syncthreads();
+  // left-looking Cholesky: column j from the columns before it
   for (int j = 0; j < D; ++j) {
     if (t == 0) {
-      double a = L[j * D + j];
-      for (int k = 0; k < j; ++k) a -= L[j * D + k] * L[j * D + k];
-      if (!(a > 0.0)) { bad = 1; a = 1.0; }
-      L[j * D + j] = sqrt(a);
+      double a = Ls[j * D + j];
+      for (int k = 0; k < j; ++k) a -= Ls[j * D + k] * Ls[j * D + k];
+      if (!(a > 0.0)) {
+        bad = 1;
+        a = 1.0;
+      }
+      Ls[j * D + j] = sqrt(a);
     }
     __syncthreads();
+    const double djj = Ls[j * D + j];
     for (int i = j + 1 + t; i < D; i += blockDim.x) {
-      double a = L[i * D + j];
-      for (int k = 0; k < j; ++k) a -= L[i * D + k] * L[j * D + k];
-      L[i * D + j] = a / L[j * D + j];
+      double a = Ls[i * D + j];
+      for (int k = 0; k < j; ++k) a -= Ls[i * D + k] * Ls[j * D + k];
+      Ls[i * D + j] = a / djj;
     }
     __syncthreads();
   }
   if (t == 0) {
     double ld = 0.0;
-    for (int j = 0; j < D; ++j) ld += log(L[j * D + j]);
+    for (int j = 0; j < D; ++j) ld += log(Ls[j * D + j]);
     *logdet = 2.0 * ld;
     if (bad) atomicOr(status, ST_NONFINITE);
   }
-  // column t of Sigma^-1
-  for (int j = t; j < D; j += blockDim.x) {
-    double* y = work + static_cast<int64_t>(j) * D;
-    for (int i = 0; i < D; ++i) {
-      double a = i == j ? 1.0 : 0.0;
-      for (int k = 0; k < i; ++k) a -= L[i * D + k] * y[k];
-      y[i] = a / L[i * D + i];
-    }
-    for (int i = D - 1; i >= 0; --i) {
-      double a = y[i];
-      for (int k = i + 1; k < D; ++k) a -= L[k * D + i] * y[k];
-      y[i] = a / L[i * D + i];
-    }
-    for (int i = 0; i < D; ++i) sinv[static_cast<int64_t>(i) * D + j] = y[i];
+  for (int i = t; i < D * D; i += blockDim.x) L[i] = (i % D) <= (i / D) ? Ls[i] : 0.0;
+}
+
+// Column j of Sigma^-1 = L^-T L^-1 e_j, one block of 128 threads per column
+// (fp64 is scarce on this GPU: spreading the D solves over D SMs keeps them
+// short).  Forward then backward substitution; each step's dot product is
+// split over the threads (thread t takes k = t, t + 128, ...) and summed in a
+// fixed order (warp shuffles, then the four warps in order).
+__global__ void __launch_bounds__(128) tied_inv_kernel(const double* __restrict__ L, int D,
+                                                       double* __restrict__ sinv) {
+  __shared__ double y[kMaxD];
+  __shared__ double wsum[4];
+  const int j = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  auto block_sum = [&](double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) wsum[warp] = v;
+    __syncthreads();
+    const double s = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
+    __syncthreads();
+    return s;
+  };
+  for (int i = 0; i < D; ++i) {
+    double part = 0.0;
+    for (int k = t; k < i; k += 128) part += L[static_cast<int64_t>(i) * D + k] * y[k];
+    const double s = block_sum(part);
+    if (t == 0) y[i] = ((i == j ? 1.0 : 0.0) - s) / L[static_cast<int64_t>(i) * D + i];
+    __syncthreads();
   }
+  for (int i = D - 1; i >= 0; --i) {
+    double part = 0.0;
+    for (int k = i + 1 + t; k < D; k += 128) part += L[static_cast<int64_t>(k) * D + i] * y[k];
+    const double s = block_sum(part);
+    if (t == 0) y[i] = (y[i] - s) / L[static_cast<int64_t>(i) * D + i];
+    __syncthreads();
+  }
+  for (int i = t; i < D; i += 128) sinv[static_cast<int64_t>(i) * D + j] = y[i];
 }
 
 // G = sum over the partials of the CTAs in a fixed order, in fp64, with the
@@ -1450,35 +1478,53 @@ __global__ void gram_reduce_kernel(const double* __restrict__ part, int n_parts,
   G[e] = s * is * is;
 }
 
-// Shared covariance of the M-step (one block per row d, thread e = column):
+// Shared covariance of the M-step, one block of 16 x 16 threads per 16 x 16
+// tile of Sigma' (thread = element (d, e)):
 //   Sigma'_de = (G_de - sum_k N_k nu_kd nu_ke) / N, diagonal floored and
-//   regularised.  Block 0 also subtracts 1/2 tr(Sigma^-1 G) from the
-//   log-likelihood (the logits' dropped per-point term), when ll is given.
-__global__ void sigma_tied_kernel(const double* __restrict__ G, const double* __restrict__ tied_stats, int K,
-                                  int D, int64_t N, float reg_covar, float var_floor,
-                                  const double* __restrict__ sinv, double* __restrict__ ll,
-                                  float* __restrict__ out_sigma) {
-  const int d = blockIdx.x;
-  const int e = threadIdx.x;
-  if (e < D) {
-    double s = G[static_cast<int64_t>(d) * D + e];
-    for (int k = 0; k < K; ++k) {
+//   regularised.
+// The components' (N_k, nu_k) rows are staged in shared memory 32 at a time,
+// and every element sums over k in ascending order (fp64).  Block (0, 0) also
+// subtracts 1/2 tr(Sigma^-1 G) from the log-likelihood (the logits' dropped
+// per-point term), when ll is given.
+__global__ void __launch_bounds__(256) sigma_tied_kernel(const double* __restrict__ G,
+                                                         const double* __restrict__ tied_stats, int K, int D,
+                                                         int64_t N, float reg_covar, float var_floor,
+                                                         const double* __restrict__ sinv, double* __restrict__ ll,
+                                                         float* __restrict__ out_sigma) {
+  constexpr int kT = 16, kC = 32;
+  __shared__ double a_s[kC][kT];   // N_k nu_kd, rows of this tile
+  __shared__ double b_s[kC][kT];   // nu_ke, columns of this tile
+  const int tx = threadIdx.x % kT, ty = threadIdx.x / kT;
+  const int d = blockIdx.y * kT + ty, e = blockIdx.x * kT + tx;
+  double s = 0.0;
+  for (int k0 = 0; k0 < K; k0 += kC) {
+    for (int i = threadIdx.x; i < kC * kT; i += 256) {
+      const int kk = i / kT, c = i % kT;
+      const int k = k0 + kk;
       const double* ts = tied_stats + static_cast<int64_t>(k) * (D + 1);
-      s -= ts[0] * ts[1 + d] * ts[1 + e];
+      const int dr = blockIdx.y * kT + c, ec = blockIdx.x * kT + c;
+      a_s[kk][c] = (k < K && dr < D) ? ts[0] * ts[1 + dr] : 0.0;
+      b_s[kk][c] = (k < K && ec < D) ? ts[1 + ec] : 0.0;
     }
-    s /= static_cast<double>(N);
-    if (d == e) s = (s > var_floor ? s : static_cast<double>(var_floor)) + reg_covar;
-    out_sigma[static_cast<int64_t>(d) * D + e] = static_cast<float>(s);
-  }
-  if (d == 0 && ll) {
-    __shared__ double red[128];
-    double t = 0.0;
-    for (int i = e; i < D * D; i += blockDim.x) t += sinv[i] * G[i];
-    red[e] = t;
     __syncthreads();
-    if (e == 0) {
+#pragma unroll 8
+    for (int kk = 0; kk < kC; ++kk) s += a_s[kk][ty] * b_s[kk][tx];
+    __syncthreads();
+  }
+  if (d < D && e < D) {
+    double v = (G[static_cast<int64_t>(d) * D + e] - s) / static_cast<double>(N);
+    if (d == e) v = (v > var_floor ? v : static_cast<double>(var_floor)) + reg_covar;
+    out_sigma[static_cast<int64_t>(d) * D + e] = static_cast<float>(v);
+  }
+  if (blockIdx.x == 0 && blockIdx.y == 0 && ll) {
+    __shared__ double red[256];
+    double t = 0.0;
+    for (int i = threadIdx.x; i < D * D; i += 256) t += sinv[i] * G[i];
+    red[threadIdx.x] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) {
       double tot = 0.0;
-      for (int i = 0; i < static_cast<int>(blockDim.x); ++i) tot += red[i];
+      for (int i = 0; i < 256; ++i) tot += red[i];
       *ll -= 0.5 * tot;
     }
   }
@@ -1593,6 +1639,7 @@ const void* kernel_handle(KernelId id) {
     case K_THRESH_SCAN: return reinterpret_cast<const void*>(&thresh_scan_kernel);
     case K_THRESH_SCATTER: return reinterpret_cast<const void*>(&thresh_scatter_kernel);
     case K_TIED_PREP: return reinterpret_cast<const void*>(&tied_prep_kernel);
+    case K_TIED_INV: return reinterpret_cast<const void*>(&tied_inv_kernel);
     case K_GRAM_REDUCE: return reinterpret_cast<const void*>(&gram_reduce_kernel);
     case K_SIGMA_TIED: return reinterpret_cast<const void*>(&sigma_tied_kernel);
     case K_BMAX: return reinterpret_cast<const void*>(&bmax_kernel);

@@ -40,12 +40,12 @@ enum KernelId : int {
   K_TOPM_COMBINE, K_LL_TOTAL, K_TOPM_1_1_2, K_TOPM_1_2_2, K_TOPM_2_1_1,
   K_THRESH_COUNT, K_THRESH_SCAN, K_THRESH_SCATTER,
   K_TIED_PREP, K_GRAM_REDUCE, K_SIGMA_TIED,
-  K_BMAX, K_FUSED_2_2_1, K_TOPM_2_2_1,
+  K_BMAX, K_FUSED_2_2_1, K_TOPM_2_2_1, K_TIED_INV,
 };
 
 // The tied model's Gram matrix on the tensor cores (gram.cu): kernel handle for
 // np operand pieces, nch atom columns and bf16 or f32 data; its dynamic shared
-// memory and threads per CTA.  Launch: one CTA per SM (at most one per tile),
+// memory and threads per CTA.  Launch: two CTAs per SM (at most one per tile),
 // arguments (FusedArgs, double* partials [CTA][D][D]).
 const void* gram_handle(int np, int nch, bool xb);
 size_t gram_smem(int np, int nch);

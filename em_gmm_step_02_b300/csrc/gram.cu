@@ -6,7 +6,7 @@
 // log-likelihood as -1/2 tr(Sigma^-1 G), and the M-step forms the shared
 // covariance from G and the new means.
 //
-// Per 128-point tile the transform warps write y' = y * scale as fp16 into a
+// Per 128-point tile the transform warps write y' = y * scale (no squares) as fp16 into a
 // data stage (the same 128-byte-swizzled layout as the EM kernels; PRECISE
 // adds the rounding remainder as a second piece).  The stage is a K x MN
 // matrix (K = points, MN = features) read as both operands of
@@ -30,8 +30,8 @@ namespace gmm {
 namespace {
 
 struct GramSmall {
-  uint64_t full_a[2];        // stage s filled (128 transform threads)
-  uint64_t empty_g[2][8];    // stage s, 16-row group g read by the MMAs
+  uint64_t full_a[4];        // stage s filled (128 transform threads)
+  uint64_t empty_g[4][8];    // stage s, 16-row group g read by the MMAs
   uint64_t acc_full[2];      // period sums complete in buffer b
   uint64_t acc_empty[2];     // buffer b read out (128 flush threads)
   uint64_t drain;
@@ -43,7 +43,7 @@ struct GramSmall {
 template <int NP, int NCH, int NST>
 struct GramCfg {
   static constexpr int kDp = NCH * kAtomElems;
-  static constexpr int kPieceBytes = 2 * NCH * kChunkBytes;   // [y | y^2] for 128 rows (y^2 unused here)
+  static constexpr int kPieceBytes = NCH * kChunkBytes;       // y' for 128 rows (no squares)
   static constexpr int kStageBytes = NP * kPieceBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffSmall = NST * kStageBytes;
@@ -52,8 +52,10 @@ struct GramCfg {
 
 constexpr int kGramThreads = 288;   // transform 0-3, MMA 4, flush 5-8
 
+// Two CTAs per SM (256 tensor-memory columns each): twice the rows in flight
+// from HBM.
 template <int NP, int NCH, int NST, bool XB>
-__global__ void __launch_bounds__(kGramThreads, 1) gram_tc_kernel(const FusedArgs a, double* __restrict__ part) {
+__global__ void __launch_bounds__(kGramThreads, 2) gram_tc_kernel(const FusedArgs a, double* __restrict__ part) {
   using CF = GramCfg<NP, NCH, NST>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -68,9 +70,11 @@ __global__ void __launch_bounds__(kGramThreads, 1) gram_tc_kernel(const FusedArg
   if (tid == 0) {
     S->abort_flag = 0;
     S->poll_limit = a.max_polls ? a.max_polls : kMaxPolls;
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&S->full_a[i], 128);
       for (int g = 0; g < 8; ++g) mbar_init(&S->empty_g[i][g], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&S->acc_full[i], 1);
       mbar_init(&S->acc_empty[i], 128);
     }
@@ -87,7 +91,8 @@ __global__ void __launch_bounds__(kGramThreads, 1) gram_tc_kernel(const FusedArg
   const uint32_t tmem = S->tmem_base;
 
   if (warp < 4) {
-    transform_warps<CF, GramSmall, NP, NCH, NST, XB, false>(a, sm, S, abort_flag, tid, tgroup, n_tgroups, my_tiles);
+    transform_warps<CF, GramSmall, NP, NCH, NST, XB, false, false>(a, sm, S, abort_flag, tid, tgroup, n_tgroups,
+                                                                   my_tiles);
   } else if (warp == 4) {
     if (lane == 0) {
       const uint32_t sA = smem_u32(sm + CF::kOffA);
@@ -163,14 +168,15 @@ const void* gram_fn_t(bool xb) {
 
 }  // namespace
 
-// FAST: one fp16 piece, two stages; PRECISE: two pieces (one stage at D > 64).
+// Stages of y' only (no squares), sized for two CTAs per SM: FAST three
+// stages, PRECISE (two pieces) two at D <= 64, one above.
 const void* gram_handle(int np, int nch, bool xb) {
-  if (np == 1) return nch == 1 ? gram_fn_t<1, 1, 2>(xb) : gram_fn_t<1, 2, 2>(xb);
+  if (np == 1) return nch == 1 ? gram_fn_t<1, 1, 3>(xb) : gram_fn_t<1, 2, 3>(xb);
   return nch == 1 ? gram_fn_t<2, 1, 2>(xb) : gram_fn_t<2, 2, 1>(xb);
 }
 
 size_t gram_smem(int np, int nch) {
-  size_t b = np == 1 ? (nch == 1 ? GramCfg<1, 1, 2>::kEnd : GramCfg<1, 2, 2>::kEnd)
+  size_t b = np == 1 ? (nch == 1 ? GramCfg<1, 1, 3>::kEnd : GramCfg<1, 2, 3>::kEnd)
                      : (nch == 1 ? GramCfg<2, 1, 2>::kEnd : GramCfg<2, 2, 1>::kEnd);
   return b + 1024;
 }

@@ -28,7 +28,9 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
 // Thread `tid` owns one 8-feature unit of every RPP-th row.  All loads of a
 // tile are issued together (and, when the registers allow, one tile ahead)
 // so that the whole tile is in flight at once.
-template <typename CF, typename SmallT, int NP, int NCH, int NST, bool XB, bool kTopm>
+// kSq = false writes x' only (the Gram matrix needs no squares; its stage
+// holds one 64-feature block column per atom and no x'^2 part).
+template <typename CF, typename SmallT, int NP, int NCH, int NST, bool XB, bool kTopm, bool kSq = true>
 __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm, SmallT* S,
                                                 volatile uint32_t* abort_flag, int tid, int tgroup,
                                                 int n_tgroups, int my_tiles) {
@@ -121,7 +123,7 @@ __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm,
           hq.z = pack_f16x2(x[4] * x[4], x[5] * x[5]); hq.w = pack_f16x2(x[6] * x[6], x[7] * x[7]);
         }
         *reinterpret_cast<uint4*>(stage + off) = hx;
-        *reinterpret_cast<uint4*>(stage + off2) = hq;
+        if constexpr (kSq) *reinterpret_cast<uint4*>(stage + off2) = hq;
       } else {
         float xh[8], xl[8], qh[8], ql[8];
 #pragma unroll
@@ -136,15 +138,19 @@ __device__ __forceinline__ void transform_warps(const FusedArgs& a, uint8_t* sm,
         v.x = pack_f16x2(xh[0], xh[1]); v.y = pack_f16x2(xh[2], xh[3]);
         v.z = pack_f16x2(xh[4], xh[5]); v.w = pack_f16x2(xh[6], xh[7]);
         *reinterpret_cast<uint4*>(stage + off) = v;
-        v.x = pack_f16x2(qh[0], qh[1]); v.y = pack_f16x2(qh[2], qh[3]);
-        v.z = pack_f16x2(qh[4], qh[5]); v.w = pack_f16x2(qh[6], qh[7]);
-        *reinterpret_cast<uint4*>(stage + off2) = v;
+        if constexpr (kSq) {
+          v.x = pack_f16x2(qh[0], qh[1]); v.y = pack_f16x2(qh[2], qh[3]);
+          v.z = pack_f16x2(qh[4], qh[5]); v.w = pack_f16x2(qh[6], qh[7]);
+          *reinterpret_cast<uint4*>(stage + off2) = v;
+        }
         v.x = pack_f16x2(xl[0], xl[1]); v.y = pack_f16x2(xl[2], xl[3]);
         v.z = pack_f16x2(xl[4], xl[5]); v.w = pack_f16x2(xl[6], xl[7]);
         *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off) = v;
-        v.x = pack_f16x2(ql[0], ql[1]); v.y = pack_f16x2(ql[2], ql[3]);
-        v.z = pack_f16x2(ql[4], ql[5]); v.w = pack_f16x2(ql[6], ql[7]);
-        *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off2) = v;
+        if constexpr (kSq) {
+          v.x = pack_f16x2(ql[0], ql[1]); v.y = pack_f16x2(ql[2], ql[3]);
+          v.z = pack_f16x2(ql[4], ql[5]); v.w = pack_f16x2(ql[6], ql[7]);
+          *reinterpret_cast<uint4*>(stage + CF::kPieceBytes + off2) = v;
+        }
       }
     }
   };
