@@ -53,6 +53,7 @@ def _both(w, X, chunk_rows, precision="auto"):
     (3001, 48, 40, "diag", "f32", 640),          # PRECISE
     (12000, 32, 1100, "diag", "bf16", 4000),     # two-pass plan per chunk; 4000 -> 3968 rows
     (4096, 64, 256, "spherical", "f32", 128),    # 32 one-tile chunks
+    (3000, 128, 100, "diag", "f32", 1024),       # PRECISE with the streamed parameter image
 ])
 def test_host_stream_matches_device_step_and_oracle(N, D, K, cov, xd, chunk):
     w = W.generic(N, D, K, cov, xd, seed=N + K)

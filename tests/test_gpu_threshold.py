@@ -56,6 +56,7 @@ def _run(X_cpu, lw, mu, var, cov, tau, m, **kw):
     (4096, 8, 16, "diag", "f32", 0.05, 16),
     (12000, 32, 1100, "diag", "bf16", 0.2, 4),      # two-pass plan
     (5000, 64, 256, "spherical", "f32", 0.3, 3),
+    (3000, 128, 100, "diag", "f32", 0.2, 4),         # PRECISE, 128 features
 ])
 def test_threshold_against_oracle(N, D, K, cov, xd, tau, m):
     w = W.generic(N, D, K, cov, xd, seed=N + 5 * D + K)
