@@ -902,7 +902,9 @@ const void* emfast_handle_nch(int mode, int maxm) {
       if (maxm <= 2) return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_TOPM, 2>);
       if (maxm <= 4) return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_TOPM, 4>);
       return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_TOPM, 8>);
-    default: return reinterpret_cast<const void*>(&em_fast_kernel<NCH, MODE_EM, 0>);
+    // the single-pass EM step runs on the fused kernel (gmm_kernels.cu), which
+    // measured faster than this kernel in that mode
+    default: return nullptr;
   }
 }
 

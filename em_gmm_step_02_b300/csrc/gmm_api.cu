@@ -190,7 +190,7 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
   p.F = 2 * p.nch * kAtomElems + 1;
   p.flush = p.fast ? 128 : 16;
   const int sms = need_device ? device_sms() : 148;
-  const void* fn = p.emfast ? emfast_handle(p.nch, p.two_pass ? MODE_LSE : MODE_EM) : fused_fn(p.np, p.nch, p.nst);
+  const void* fn = p.emfast ? emfast_handle(p.nch, MODE_LSE) : fused_fn(p.np, p.nch, p.nst);
   if (!p.two_pass) {
     p.C = p.n_slices;
     p.n_kgroups = 1;

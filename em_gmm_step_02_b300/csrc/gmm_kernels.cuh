@@ -52,8 +52,9 @@ size_t gram_smem(int np, int nch);
 int gram_threads();
 
 // Handles of the two-team FAST kernels (em_fast.cu), nch = 1 or 2, one per
-// mode (MODE_EM, MODE_LSE, MODE_GIVEN, MODE_TOPM with candidate lists of
-// maxm = 2, 4 or 8), and their dynamic shared-memory size (512 threads per CTA).
+// mode (MODE_LSE, MODE_GIVEN, MODE_TOPM with candidate lists of maxm = 2, 4
+// or 8; NULL for MODE_EM, which runs on the fused kernel), and their dynamic
+// shared-memory size (512 threads per CTA).
 const void* emfast_handle(int nch, int mode, int maxm = 0);
 size_t emfast_smem(int nch);
 constexpr int kEmFastThreads = 512;
