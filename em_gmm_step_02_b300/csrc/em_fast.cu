@@ -410,6 +410,36 @@ __device__ __forceinline__ void bitonic_keep_min(float (&a)[MAXM], const float (
       }
 }
 
+// Merge four keys into a sorted list of MAXM, keeping the MAXM smallest
+// (ascending).  The four are first sorted (a five-comparator network); then,
+// as in bitonic_keep_min with the four padded by +inf to MAXM, the list's tail
+// takes the elementwise minimum with the four reversed (only the two smallest
+// matter when MAXM = 2) and half-cleaners sort the resulting bitonic sequence.
+// Per key this costs 5.5 (MAXM = 4) or 9.5 (MAXM = 8) min/max operations
+// instead of 2 MAXM for an insertion into the sorted list.
+template <int MAXM>
+__device__ __forceinline__ void merge_four(float (&a)[MAXM], float q0, float q1, float q2, float q3) {
+  auto ce = [](float& x, float& y) {
+    const float lo = fminf(x, y);
+    y = fmaxf(x, y);
+    x = lo;
+  };
+  ce(q0, q1);
+  ce(q2, q3);
+  ce(q0, q2);
+  ce(q1, q3);
+  ce(q1, q2);
+  const float q[4] = {q0, q1, q2, q3};
+  constexpr int kTail = MAXM < 4 ? MAXM : 4;
+#pragma unroll
+  for (int i = 0; i < kTail; ++i) a[MAXM - 1 - i] = fminf(a[MAXM - 1 - i], q[i]);
+#pragma unroll
+  for (int stride = MAXM / 2; stride >= 1; stride >>= 1)
+#pragma unroll
+    for (int i = 0; i < MAXM; ++i)
+      if ((i & stride) == 0) ce(a[i], a[i + stride]);
+}
+
 // ------------------------------------------------------------------ top-m teams
 // MODE_TOPM: each point's m largest responsibilities (over every component of
 // the launch's K group) and their components, best first, ties to the lower
@@ -492,14 +522,15 @@ __device__ __forceinline__ void topm_team_loop(const FusedArgs& a, uint8_t* sm, 
       for (int e = 0; e < 32; ++e) {
         if (live) sq[e & 3] += ex2(fmaf(v[e], is, off));
         const float d = live ? fminf(M - v[e], 1e30f) : 1e30f;
-        float x = __uint_as_float((__float_as_uint(d) & ~127u) | static_cast<uint32_t>(32 * c + e));
-#pragma unroll
-        for (int s = 0; s < MAXM; ++s) {
-          const float lo = fminf(x, key[e & 3][s]);
-          x = fmaxf(x, key[e & 3][s]);
-          key[e & 3][s] = lo;
-        }
+        v[e] = __uint_as_float((__float_as_uint(d) & ~127u) | static_cast<uint32_t>(32 * c + e));
       }
+      // stream st takes columns st, st + 4, ..., st + 28 of the chunk, in two
+      // groups of four
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+          merge_four<MAXM>(key[st], v[st + 16 * g], v[st + 16 * g + 4], v[st + 16 * g + 8], v[st + 16 * g + 12]);
     }
     // the logit buffer is free for tile j + 2
     tc_fence_before();
