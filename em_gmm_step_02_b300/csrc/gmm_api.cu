@@ -695,7 +695,7 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
 
 // Approximate top-k EM: workspace placed from byte `base` on -- the top-k
 // lists (responsibilities, components) of every point, the counting sort's
-// per-(component, tile) counts, per-component totals and offsets, the sorted
+// per-(tile, component) counts, per-component totals and offsets, the sorted
 // pairs, the per-chunk partial statistics and N_k, then the top-m pass's
 // own space.
 struct TopkSpace {
@@ -709,9 +709,9 @@ struct TopkSpace {
 TopkSpace topk_space(const Plan& p, int k, size_t base) {
   TopkSpace t;
   const size_t nk = static_cast<size_t>(p.N) * k;
-  // 512 points per tile (short serial walks), doubled while the count table
-  // K x tiles would exceed 2^25 entries
-  t.tile = 512;
+  // 4096 points per tile (the walks count in shared memory), doubled while the
+  // count table tiles x K would exceed 2^25 entries
+  t.tile = 4096;
   while (static_cast<int64_t>(p.K) * ((p.N + t.tile - 1) / t.tile) > (int64_t(1) << 25)) t.tile *= 2;
   t.T = (p.N + t.tile - 1) / t.tile;
   t.max_chunks = static_cast<int64_t>(nk / kTkChunk) + p.K + 1;
@@ -757,18 +757,20 @@ int run_topk_mstep(const Plan& p, const void* X, int k, const gmm_opts& o, uint8
   double* part = reinterpret_cast<double*>(ws + t.off_part);
   const int32_t* idx = reinterpret_cast<const int32_t*>(ws + t.off_i);
   const float* resp = reinterpret_cast<const float*>(ws + t.off_r);
-  const unsigned tile_blocks = static_cast<unsigned>((t.T + 7) / 8);
+  const unsigned tile_blocks = static_cast<unsigned>(t.T);
+  const size_t table_bytes = sizeof(int32_t) * static_cast<size_t>(p.K);
+  if ((r = set_smem_attr(topk_handle(TK_COUNT, xb), table_bytes))) return r;
+  if ((r = set_smem_attr(topk_handle(TK_FILL, xb), table_bytes))) return r;
   const unsigned chunk_blocks = static_cast<unsigned>(t.max_chunks);
-  CUDA_TRY(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * static_cast<size_t>(p.K) * t.T, s));
-  if ((r = launch(topk_handle(TK_COUNT, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, p.N, k, p.K, t.T, t.tile,
-                  cnt)))
+  if ((r = launch(topk_handle(TK_COUNT, xb), dim3(tile_blocks), dim3(32), table_bytes, s, 1, idx, p.N, k, p.K, t.T,
+                  t.tile, cnt)))
     return r;
-  if ((r = launch(topk_handle(TK_SCAN, xb), dim3(p.K), dim3(256), 0, s, 1, cnt, t.T, tot))) return r;
+  if ((r = launch(topk_handle(TK_SCAN, xb), dim3((p.K + 31) / 32), dim3(1024), 0, s, 1, cnt, p.K, t.T, tot))) return r;
   if ((r = launch(topk_handle(TK_BASE, xb), dim3(1), dim3(1024), 0, s, 1, static_cast<const int32_t*>(tot), p.K,
                   base, cbase)))
     return r;
-  if ((r = launch(topk_handle(TK_FILL, xb), dim3(tile_blocks), dim3(256), 0, s, 1, idx, resp, p.N, k, p.K, t.T,
-                  t.tile, cnt, static_cast<const int64_t*>(base), pt, rw)))
+  if ((r = launch(topk_handle(TK_FILL, xb), dim3(tile_blocks), dim3(32), table_bytes, s, 1, idx, resp, p.N, k, p.K,
+                  t.T, t.tile, static_cast<const int32_t*>(cnt), static_cast<const int64_t*>(base), pt, rw)))
     return r;
   // 16-byte row loads when a row is a whole number of 16-byte units
   const bool vec = (p.D * (xb ? 2 : 4)) % 16 == 0;

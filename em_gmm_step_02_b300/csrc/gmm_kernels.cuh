@@ -63,8 +63,9 @@ constexpr int kEmFastThreads = 512;
 constexpr int kThreshBlock = 256;
 
 // Approximate top-k EM (topk_em.cu): pairs per chunk of the statistics
-// kernel and the kernels.  Launch shapes: COUNT and FILL one warp per tile of
-// points (256 threads per CTA); SCAN one CTA of 256 per component; BASE one
+// kernel and the kernels.  Launch shapes: COUNT and FILL one CTA of 32 threads
+// per tile of points with K * 4 bytes of dynamic shared memory; SCAN one CTA
+// of 1024 per 32 components; BASE one
 // CTA of 1024; STATS / STATS_VEC one CTA of 128 per chunk (chunks beyond the
 // device-side total return at once; partials of 3 D + 1 doubles per chunk;
 // STATS_VEC for rows of a multiple of 16 bytes); FINAL one CTA of 128 per

@@ -11,10 +11,10 @@
 // sparse: point i adds to k components only.  They are gathered, not
 // scattered, so that every sum has one fixed order:
 //   1. tk_count:  a stable counting sort of the N k (point, component) pairs
-//                 by component.  Points are cut into tiles (512 points, more
+//                 by component.  Points are cut into tiles (4096 points, more
 //                 when K times the number of tiles would pass 2^25); one warp
 //                 walks one tile in point order and counts its pairs per
-//                 component (counts[c][t]).
+//                 component in shared memory (counts[t][c]).
 //   2. tk_scan:   per component, the exclusive prefix over tiles; the total.
 //   3. tk_base:   the exclusive prefix over components (pair offsets) and the
 //                 chunking of every component's pairs into runs of kTkChunk.
@@ -56,53 +56,64 @@ __device__ __forceinline__ int pair_comp(const int32_t* __restrict__ idx, int64_
   return (c >= 0 && c < K) ? c : -1;
 }
 
-// One warp per tile: counts[c * T + t] = pairs of tile t with component c.
-// The warp owns column t alone, so plain read-modify-writes suffice; the
-// warp barrier orders them between steps.
-__global__ void __launch_bounds__(256) tk_count_kernel(const int32_t* __restrict__ idx, int64_t N, int k, int K,
-                                                       int64_t T, int tile, int32_t* __restrict__ counts) {
-  const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+// One warp (one CTA of 32 threads) per tile: counts[t * K + c] = pairs of
+// tile t with component c, counted in a table of K ints in shared memory
+// (dynamic, K * 4 bytes).  The warp walks its tile in point order; lanes with
+// equal components form a group whose highest lane adds the group's size; the
+// warp barrier orders the table updates between steps.
+__global__ void __launch_bounds__(32) tk_count_kernel(const int32_t* __restrict__ idx, int64_t N, int k, int K,
+                                                      int64_t T, int tile, int32_t* __restrict__ counts) {
+  extern __shared__ int32_t table[];
+  const int64_t t = blockIdx.x;
+  const int lane = threadIdx.x;
+  for (int c = lane; c < K; c += 32) table[c] = 0;
+  __syncwarp();
   const int64_t q0 = t * tile * k;
   const int64_t q1 = (t + 1) * tile < N ? (t + 1) * tile * k : N * k;
   for (int64_t b = q0; b < q1; b += 32) {
     const int c = pair_comp(idx, b + lane, q1, K);
     const unsigned grp = __match_any_sync(0xffffffffu, c);
-    if (c >= 0 && lane == 31 - __clz(grp)) counts[static_cast<int64_t>(c) * T + t] += __popc(grp);
+    if (c >= 0 && lane == 31 - __clz(grp)) table[c] += __popc(grp);
     __syncwarp();
   }
+  int32_t* row = counts + t * K;
+  for (int c = lane; c < K; c += 32) row[c] = table[c];
 }
 
-// One CTA per component: exclusive prefix of counts[c][0 .. T) in place,
-// the total into tot[c].
-__global__ void __launch_bounds__(256) tk_scan_kernel(int32_t* __restrict__ counts, int64_t T,
-                                                      int32_t* __restrict__ tot) {
-  __shared__ int32_t wsum[8];
-  __shared__ int32_t carry;
-  const int c = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int32_t* row = counts + static_cast<int64_t>(c) * T;
-  if (tid == 0) carry = 0;
+// Per component c, the exclusive prefix of counts[0 .. T)[c] over the tiles,
+// in place, and the total into tot[c].  One CTA of 32 x 32 threads per 32
+// components: thread (x, y) takes component 32 * blockIdx.x + x and the y-th
+// segment of the tiles (loads of one tile row are consecutive); the segment
+// sums are scanned in segment order, then each segment is rewritten.
+__global__ void __launch_bounds__(1024) tk_scan_kernel(int32_t* __restrict__ counts, int K, int64_t T,
+                                                       int32_t* __restrict__ tot) {
+  __shared__ int32_t seg_sum[32][33];
+  const int x = threadIdx.x & 31, y = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + x;
+  const int64_t S = (T + 31) / 32;
+  const int64_t t0 = y * S, t1 = min(T, t0 + S);
+  int32_t s = 0;
+  if (c < K)
+    for (int64_t t = t0; t < t1; ++t) s += counts[t * K + c];
+  seg_sum[y][x] = s;
   __syncthreads();
-  for (int64_t b = 0; b < T; b += 256) {
-    const int64_t t = b + tid;
-    const int32_t v = t < T ? row[t] : 0;
-    int32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+  if (y == 0) {
+    int32_t run = 0;
+    for (int g = 0; g < 32; ++g) {
+      const int32_t v = seg_sum[g][x];
+      seg_sum[g][x] = run;
+      run += v;
     }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    int32_t before = carry;
-    for (int w = 0; w < warp; ++w) before += wsum[w];
-    if (t < T) row[t] = before + x - v;
-    __syncthreads();
-    if (tid == 255) carry = before + x;
-    __syncthreads();
+    if (c < K) tot[c] = run;
   }
-  if (tid == 0) tot[c] = carry;
+  __syncthreads();
+  int32_t run = seg_sum[y][x];
+  if (c < K)
+    for (int64_t t = t0; t < t1; ++t) {
+      const int32_t v = counts[t * K + c];
+      counts[t * K + c] = run;
+      run += v;
+    }
 }
 
 // One CTA of 1024 threads: base[c] = sum of tot over components below c
@@ -146,17 +157,22 @@ __global__ void __launch_bounds__(1024) tk_base_kernel(const int32_t* __restrict
   }
 }
 
-// One warp per tile, the same walk as tk_count: every pair goes to
-// base[c] + (pairs of c in earlier tiles) + (pairs of c earlier in this
-// tile).  counts[c][t] (the exclusive prefix) is advanced as the cursor.
-// The responsibility is normalised over the point's k kept components.
-__global__ void __launch_bounds__(256) tk_fill_kernel(const int32_t* __restrict__ idx, const float* __restrict__ resp,
-                                                      int64_t N, int k, int K, int64_t T, int tile,
-                                                      int32_t* __restrict__ counts, const int64_t* __restrict__ base,
-                                                      uint32_t* __restrict__ pt, float* __restrict__ rw) {
-  const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+// One warp (one CTA of 32 threads) per tile, the same walk as tk_count: every
+// pair goes to base[c] + (pairs of c in earlier tiles) + (pairs of c earlier
+// in this tile).  The tile's row of the scanned counts is the cursor table in
+// shared memory (K ints).  The responsibility is normalised over the point's k
+// kept components.
+__global__ void __launch_bounds__(32) tk_fill_kernel(const int32_t* __restrict__ idx, const float* __restrict__ resp,
+                                                     int64_t N, int k, int K, int64_t T, int tile,
+                                                     const int32_t* __restrict__ counts,
+                                                     const int64_t* __restrict__ base, uint32_t* __restrict__ pt,
+                                                     float* __restrict__ rw) {
+  extern __shared__ int32_t table[];
+  const int64_t t = blockIdx.x;
+  const int lane = threadIdx.x;
+  const int32_t* row = counts + t * K;
+  for (int c = lane; c < K; c += 32) table[c] = row[c];
+  __syncwarp();
   const int64_t q0 = t * tile * k;
   const int64_t q1 = (t + 1) * tile < N ? (t + 1) * tile * k : N * k;
   for (int64_t b = q0; b < q1; b += 32) {
@@ -166,17 +182,17 @@ __global__ void __launch_bounds__(256) tk_fill_kernel(const int32_t* __restrict_
     int32_t cur = 0;
     if (c >= 0) {
       const int64_t i = q / k;
-      const float* row = resp + i * k;
+      const float* rrow = resp + i * k;
       float s = 0.f;
-      for (int j = 0; j < k; ++j) s += __ldg(row + j);
+      for (int j = 0; j < k; ++j) s += __ldg(rrow + j);
       const float r = __ldg(resp + q);
-      cur = counts[static_cast<int64_t>(c) * T + t];
+      cur = table[c];
       const int64_t pos = base[c] + cur + __popc(grp & lanemask_lt());
       pt[pos] = static_cast<uint32_t>(i);
       rw[pos] = s > 0.f ? r / s : 0.f;
     }
     __syncwarp();
-    if (c >= 0 && lane == 31 - __clz(grp)) counts[static_cast<int64_t>(c) * T + t] = cur + __popc(grp);
+    if (c >= 0 && lane == 31 - __clz(grp)) table[c] = cur + __popc(grp);
     __syncwarp();
   }
 }
