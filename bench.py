@@ -332,7 +332,7 @@ def run_ours(args, w, ws, rank, local):
         e2e_ms = max_over_ranks(ws, e0.elapsed_time(e1) / args.steps)
         e2e = {"value": ws * 1e3 / e2e_ms, "unit": "EM iter/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
-               "api": "gmm_em_step_host: X from pinned host memory in 4M-row chunks, copies overlapped"}
+               "api": "gmm_em_step_host: X from pinned host memory in chunks of the default 1M rows, copies overlapped"}
         del Xh
 
     if rank != 0:

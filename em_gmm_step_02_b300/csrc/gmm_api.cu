@@ -77,8 +77,11 @@ struct Plan {
 };
 
 constexpr int kCombineBlocks = 296;
-// default rows per chunk of the host-data entry point (1 GiB of bf16 rows at D = 128)
-constexpr int64_t kHostChunkRows = int64_t(1) << 22;
+// default rows per chunk of the host-data entry point (256 MiB of bf16 rows at
+// D = 128): the last chunk's kernels are the part of a step that no copy
+// overlaps, so smaller chunks bring the step closer to the host link's time
+// (10M x 128 bf16: 47.3 ms per step at 2^20 rows, 51.0 ms at 2^22)
+constexpr int64_t kHostChunkRows = int64_t(1) << 20;
 constexpr size_t kStatusBytes = 256;
 
 int device_sms() {

@@ -215,7 +215,7 @@ int gmm_assign_threshold(const void *X, int64_t N, int32_t D, int32_t K, int32_t
  *    asynchronously.  Parameters and outputs are device pointers exactly as
  *    for gmm_em_step; they may alias the same way.
  *  - The rows go to the GPU in chunks of chunk_rows rows (rounded down to a
- *    multiple of 128; 0 picks 4,194,304) through two device staging buffers:
+ *    multiple of 128; 0 picks 1,048,576) through two device staging buffers:
  *    chunk c + 1 is copied on an internal stream while chunk c is processed
  *    on `stream`.  The statistics of all chunks add into the same partials,
  *    so the result equals one gmm_em_step over all N rows up to the order of
