@@ -235,7 +235,9 @@ __device__ __forceinline__ void team_loop(const FusedArgs& a, uint8_t* sm, FastS
         }
         lse = s2 > 0.f ? mx + lg2(s2) : -CUDART_INF_F;
       }
-      if (rank == 0 && valid) a.lse_part[static_cast<int64_t>(blockIdx.y) * a.N + n] = lse;
+      // K group of this CTA: the slice itself without clusters (slice-major grid)
+      const int64_t kgroup = C == 1 ? blockIdx.x : blockIdx.y;
+      if (rank == 0 && valid) a.lse_part[kgroup * a.N + n] = lse;
       continue;
     } else {
       // ---- local online softmax over this CTA's 128 components
@@ -803,8 +805,12 @@ __global__ void __launch_bounds__(512, 1) em_fast_kernel(const FusedArgs a) {
   constexpr bool stats = MODE == MODE_EM || MODE == MODE_GIVEN;
   const int C = a.C;
 
+  // The statistics pass, and the normaliser pass without clusters, launch
+  // slice-major (blockIdx.x = slice): the CTAs that run at the same time share
+  // their point tiles, which then come from L2 once per tile group instead of
+  // once per slice.
   int rank, slice, tgroup, n_tgroups;
-  if (given) {
+  if (given || (MODE == MODE_LSE && C == 1)) {
     rank = 0;
     slice = blockIdx.x;
     tgroup = blockIdx.y;

@@ -526,9 +526,10 @@ int run_estep(const Plan& p, const FusedArgs& a, uint8_t* ws, double* ll_part, c
     FusedArgs a1 = a;
     a1.mode = MODE_LSE;
     a1.C = p.C1e;
-    if ((r = launch_main(estep_fn(p, MODE_LSE), dim3(p.C1e * p.tg1e, p.n_kgroups_e), dim3(p.threads), p.smem, s,
-                         p.C1e, a1)))
-      return r;
+    // without clusters the two-team kernel takes a slice-major grid (the CTAs
+    // that run together share their point tiles in L2)
+    const dim3 g1 = (p.emfast && p.C1e == 1) ? dim3(p.n_kgroups_e, p.tg1e) : dim3(p.C1e * p.tg1e, p.n_kgroups_e);
+    if ((r = launch_main(estep_fn(p, MODE_LSE), g1, dim3(p.threads), p.smem, s, p.C1e, a1))) return r;
     float* lse = reinterpret_cast<float*>(ws + p.off_lse);
     if ((r = launch(kernel_handle(K_LSE_COMBINE), dim3(kCombineBlocks), dim3(256), 0, s, 1,
                     static_cast<const float*>(a.lse_part), p.n_kgroups_e, p.N, lse, ll_part)))
