@@ -137,6 +137,14 @@ __device__ __forceinline__ void team_loop(const FusedArgs& a, uint8_t* sm, FastS
   const bool ll_row = MODE == MODE_EM && (nl % C) == rank;
   double ll = 0.0;
   float llf = 0.f;
+  // MODE_GIVEN: the row normaliser of the team's next tile is loaded one tile
+  // ahead, off the critical path of the current one
+  auto lse_of = [&](int jt) {
+    const int64_t nn = static_cast<int64_t>(tgroup + jt * n_tgroups) * kBN + nl;
+    return (jt < my_tiles && nn < a.N) ? __ldg(a.lse_in + nn) : -CUDART_INF_F;
+  };
+  float lse_next = 0.f;
+  if constexpr (given) lse_next = lse_of(t);
   for (int j = t; j < my_tiles; j += 2) {
     const int jj = j >> 1;
     const int64_t n = static_cast<int64_t>(tgroup + j * n_tgroups) * kBN + nl;
@@ -144,11 +152,16 @@ __device__ __forceinline__ void team_loop(const FusedArgs& a, uint8_t* sm, FastS
     uint32_t pk[64];                         // packed fp16 pairs of p (chunk c: pk[16c .. 16c + 15])
     float Mc[4];                             // running row maximum (accumulator units) after chunk c
     float lse;                               // row normaliser, log2 units
+    float lse_cur = 0.f;
+    if constexpr (given) {
+      lse_cur = lse_next;
+      lse_next = lse_of(j + 2);
+    }
     mbar_wait(&S->acc_full[t], static_cast<uint32_t>(jj & 1), abort_flag, a.status);
     tc_fence_after();
     if constexpr (given) {
       // normaliser over all components from memory: r * 2^10 directly
-      lse = valid ? __ldg(a.lse_in + n) : -CUDART_INF_F;
+      lse = valid ? lse_cur : -CUDART_INF_F;
       const float off = lse > -CUDART_INF_F ? kLog2R - lse : -CUDART_INF_F;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
