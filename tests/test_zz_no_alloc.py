@@ -18,6 +18,7 @@ CASES = [
     # N, D, K, cov, x_dtype, (tolerance on means/variances/weights, on log-likelihood per point)
     (20000, 128, 1024, "diag", "bf16", (2e-2, 1e-2)),
     (5000, 64, 256, "spherical", "f32", (1e-4, 1e-4)),
+    (4000, 128, 256, "diag", "f32", (1e-4, 1e-4)),     # PRECISE with the streamed parameter image
 ]
 
 
