@@ -1401,11 +1401,14 @@ __global__ void __launch_bounds__(128) tied_prep_kernel(const float* __restrict_
     Ls[i] = v;
   }
   __syncthreads();
-  // left-looking Cholesky: column j from the columns before it
+  // right-looking Cholesky: column j is final once the updates of the
+  // columns before it have been applied; it then updates the trailing lower
+  // triangle (thread t owns rows t, t + 128, ...; the updates of one row are
+  // independent of each other, so fp64, which is slow on this GPU, runs at
+  // its throughput rather than its latency)
   for (int j = 0; j < D; ++j) {
     if (t == 0) {
       double a = Ls[j * D + j];
-      for (int k = 0; k < j; ++k) a -= Ls[j * D + k] * Ls[j * D + k];
       if (!(a > 0.0)) {
         bad = 1;
         a = 1.0;
@@ -1414,10 +1417,11 @@ __global__ void __launch_bounds__(128) tied_prep_kernel(const float* __restrict_
     }
     __syncthreads();
     const double djj = Ls[j * D + j];
+    for (int i = j + 1 + t; i < D; i += blockDim.x) Ls[i * D + j] /= djj;
+    __syncthreads();
     for (int i = j + 1 + t; i < D; i += blockDim.x) {
-      double a = Ls[i * D + j];
-      for (int k = 0; k < j; ++k) a -= Ls[i * D + k] * Ls[j * D + k];
-      Ls[i * D + j] = a / djj;
+      const double lij = Ls[i * D + j];
+      for (int k = j + 1; k <= i; ++k) Ls[i * D + k] -= lij * Ls[k * D + j];
     }
     __syncthreads();
   }
