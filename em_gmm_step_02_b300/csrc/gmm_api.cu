@@ -406,13 +406,14 @@ int run_prep(const Plan& p, const void* X, const float* lw, const float* mu, con
   double* logdet = tied ? reinterpret_cast<double*>(ws + p.off_logdet) : nullptr;
   if (tied) {
     // Sigma^-1 and log|Sigma| (one block), then the Gram matrix of the data
-    const size_t lbytes = sizeof(double) * static_cast<size_t>(p.D) * p.D;
+    const size_t lbytes = sizeof(double) * static_cast<size_t>(p.D) * (p.D + 1);
     int r = set_smem_attr(kernel_handle(K_TIED_PREP), lbytes);
     if (r) return r;
     r = launch(kernel_handle(K_TIED_PREP), dim3(1), dim3(128), lbytes, s, 1, var, p.D,
                reinterpret_cast<double*>(ws + p.off_tl), logdet, status);
     if (r) return r;
-    r = launch(kernel_handle(K_TIED_INV), dim3(p.D), dim3(128), 0, s, 1,
+    if ((r = set_smem_attr(kernel_handle(K_TIED_INV), lbytes))) return r;
+    r = launch(kernel_handle(K_TIED_INV), dim3(p.D), dim3(128), lbytes, s, 1,
                static_cast<const double*>(reinterpret_cast<double*>(ws + p.off_tl)), p.D, sinv);
     if (r) return r;
     if (X) {

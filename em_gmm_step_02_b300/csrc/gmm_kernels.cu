@@ -1384,13 +1384,16 @@ __global__ void finalize_kernel(const double* __restrict__ part, int n_parts, in
 // logits returns to the log-likelihood as -1/2 tr(Sigma^-1 G).
 
 // One block of 128 threads with the Cholesky factor L of Sigma in shared
-// memory (fp64, row-major, lower; D * D * 8 bytes of dynamic shared memory):
+// memory (fp64, row-major, lower; D * (D + 1) * 8 bytes of dynamic shared memory):
 // L (written to global memory, zero above the diagonal) and log|Sigma|.  A
 // matrix that is not positive definite (or not finite) raises ST_NONFINITE.
 __global__ void __launch_bounds__(128) tied_prep_kernel(const float* __restrict__ sigma, int D,
                                                         double* __restrict__ L, double* __restrict__ logdet,
                                                         uint32_t* __restrict__ status) {
   extern __shared__ double Ls[];
+  // row stride D + 1: the threads of a step own different rows, and a
+  // stride of D doubles would put all their accesses in one bank
+  const int ld = D + 1;
   const int t = threadIdx.x;
   __shared__ int bad;
   if (t == 0) bad = 0;
@@ -1398,7 +1401,7 @@ __global__ void __launch_bounds__(128) tied_prep_kernel(const float* __restrict_
   for (int i = t; i < D * D; i += blockDim.x) {
     const float v = sigma[i];
     if (!isfinite(v)) bad = 1;
-    Ls[i] = v;
+    Ls[(i / D) * ld + i % D] = v;
   }
   __syncthreads();
   // right-looking Cholesky: column j is final once the updates of the
@@ -1406,44 +1409,60 @@ __global__ void __launch_bounds__(128) tied_prep_kernel(const float* __restrict_
   // triangle (thread t owns rows t, t + 128, ...; the updates of one row are
   // independent of each other, so fp64, which is slow on this GPU, runs at
   // its throughput rather than its latency)
+  // (scalar fp64 work is slow here: one reciprocal per column, then
+  // multiplications; the logarithms of the diagonal are taken in parallel)
+  __shared__ double rdiag;
   for (int j = 0; j < D; ++j) {
     if (t == 0) {
-      double a = Ls[j * D + j];
+      double a = Ls[j * ld + j];
       if (!(a > 0.0)) {
         bad = 1;
         a = 1.0;
       }
-      Ls[j * D + j] = sqrt(a);
+      const double r = sqrt(a);
+      Ls[j * ld + j] = r;
+      rdiag = 1.0 / r;
     }
     __syncthreads();
-    const double djj = Ls[j * D + j];
-    for (int i = j + 1 + t; i < D; i += blockDim.x) Ls[i * D + j] /= djj;
+    const double rj = rdiag;
+    for (int i = j + 1 + t; i < D; i += blockDim.x) Ls[i * ld + j] *= rj;
     __syncthreads();
     for (int i = j + 1 + t; i < D; i += blockDim.x) {
-      const double lij = Ls[i * D + j];
-      for (int k = j + 1; k <= i; ++k) Ls[i * D + k] -= lij * Ls[k * D + j];
+      const double lij = Ls[i * ld + j];
+      for (int k = j + 1; k <= i; ++k) Ls[i * ld + k] -= lij * Ls[k * ld + j];
     }
     __syncthreads();
   }
+  __shared__ double lgs[kMaxD];
+  for (int j = t; j < D; j += blockDim.x) lgs[j] = log(Ls[j * ld + j]);
+  __syncthreads();
   if (t == 0) {
-    double ld = 0.0;
-    for (int j = 0; j < D; ++j) ld += log(Ls[j * D + j]);
-    *logdet = 2.0 * ld;
+    double lg = 0.0;
+    for (int j = 0; j < D; ++j) lg += lgs[j];
+    *logdet = 2.0 * lg;
     if (bad) atomicOr(status, ST_NONFINITE);
   }
-  for (int i = t; i < D * D; i += blockDim.x) L[i] = (i % D) <= (i / D) ? Ls[i] : 0.0;
+  for (int i = t; i < D * D; i += blockDim.x) L[i] = (i % D) <= (i / D) ? Ls[(i / D) * ld + i % D] : 0.0;
 }
 
 // Column j of Sigma^-1 = L^-T L^-1 e_j, one block of 128 threads per column
 // (fp64 is scarce on this GPU: spreading the D solves over D SMs keeps them
-// short).  Forward then backward substitution; each step's dot product is
-// split over the threads (thread t takes k = t, t + 128, ...) and summed in a
-// fixed order (warp shuffles, then the four warps in order).
+// short), with L copied to shared memory (row stride D + 1, D * (D + 1) * 8
+// bytes of dynamic shared memory).  Forward then backward substitution; each
+// step's dot product is split over the threads (thread t takes k = t,
+// t + 128, ...) and summed in a fixed order (warp shuffles, then the four
+// warps in order).
 __global__ void __launch_bounds__(128) tied_inv_kernel(const double* __restrict__ L, int D,
                                                        double* __restrict__ sinv) {
+  extern __shared__ double Ls[];
   __shared__ double y[kMaxD];
+  __shared__ double rd[kMaxD];              // reciprocals of the diagonal
   __shared__ double wsum[4];
+  const int ld = D + 1;
   const int j = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int i = t; i < D * D; i += 128) Ls[(i / D) * ld + i % D] = L[i];
+  for (int i = t; i < D; i += 128) rd[i] = 1.0 / L[static_cast<int64_t>(i) * D + i];
+  __syncthreads();
   auto block_sum = [&](double v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -1455,16 +1474,16 @@ __global__ void __launch_bounds__(128) tied_inv_kernel(const double* __restrict_
   };
   for (int i = 0; i < D; ++i) {
     double part = 0.0;
-    for (int k = t; k < i; k += 128) part += L[static_cast<int64_t>(i) * D + k] * y[k];
+    for (int k = t; k < i; k += 128) part += Ls[i * ld + k] * y[k];
     const double s = block_sum(part);
-    if (t == 0) y[i] = ((i == j ? 1.0 : 0.0) - s) / L[static_cast<int64_t>(i) * D + i];
+    if (t == 0) y[i] = ((i == j ? 1.0 : 0.0) - s) * rd[i];
     __syncthreads();
   }
   for (int i = D - 1; i >= 0; --i) {
     double part = 0.0;
-    for (int k = i + 1 + t; k < D; k += 128) part += L[static_cast<int64_t>(k) * D + i] * y[k];
+    for (int k = i + 1 + t; k < D; k += 128) part += Ls[k * ld + i] * y[k];
     const double s = block_sum(part);
-    if (t == 0) y[i] = (y[i] - s) / L[static_cast<int64_t>(i) * D + i];
+    if (t == 0) y[i] = (y[i] - s) * rd[i];
     __syncthreads();
   }
   for (int i = t; i < D; i += 128) sinv[static_cast<int64_t>(i) * D + j] = y[i];
