@@ -492,7 +492,8 @@ __global__ void __launch_bounds__(128) tk_final_kernel(const double* __restrict_
   }
   constexpr double kEmpty = 1e-30;
   const bool empty = !(W >= kEmpty);
-  const double mu = d < D ? t1 / W : 0.0;
+  const double iw = 1.0 / W;   // one fp64 division per thread (fp64 is slow here), then products
+  const double mu = d < D ? t1 * iw : 0.0;
   double m2 = 0.0;
   if (!empty && d < D) {
     for (int ch = ch0; ch < ch1; ++ch) {
@@ -509,7 +510,7 @@ __global__ void __launch_bounds__(128) tk_final_kernel(const double* __restrict_
   if (cov_diag) {
     if (d < D) {
       const int64_t o = static_cast<int64_t>(c) * D + d;
-      new_vars[o] = empty ? vars[o] : static_cast<float>(fmax(m2 / W, static_cast<double>(var_floor)) + reg_covar);
+      new_vars[o] = empty ? vars[o] : static_cast<float>(fmax(m2 * iw, static_cast<double>(var_floor)) + reg_covar);
     }
   } else {
     red[d] = d < D ? m2 : 0.0;
@@ -518,7 +519,7 @@ __global__ void __launch_bounds__(128) tk_final_kernel(const double* __restrict_
       double t = 0.0;
       for (int e = 0; e < D; ++e) t += red[e];
       new_vars[c] = empty ? vars[c]
-                          : static_cast<float>(fmax(t / (static_cast<double>(D) * W), static_cast<double>(var_floor)) +
+                          : static_cast<float>(fmax(t * iw / static_cast<double>(D), static_cast<double>(var_floor)) +
                                                reg_covar);
     }
   }
