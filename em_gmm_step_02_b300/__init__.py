@@ -24,6 +24,7 @@ SPHERICAL, DIAG, TIED = 0, 1, 2
 F32, BF16 = 0, 1
 PREC = {"auto": 0, "fast": 1, "precise": 2}
 PLAN = {"auto": 0, "cluster": 1, "split": 2}
+REFINE = {"auto": 0, "on": 1, "off": 2}
 COV = {"spherical": SPHERICAL, "diag": DIAG, "tied": TIED}
 STATUS = {0: "GMM_OK", -1: "GMM_ERR_INVALID_ARG", -2: "GMM_ERR_UNSUPPORTED",
           -3: "GMM_ERR_NONFINITE", -4: "GMM_ERR_CUDA", -5: "GMM_ERR_TIMEOUT", -6: "GMM_ERR_RANGE",
@@ -40,7 +41,8 @@ class gmm_opts(ctypes.Structure):
     _fields_ = [("precision", ctypes.c_int32), ("reg_covar", ctypes.c_float),
                 ("var_floor", ctypes.c_float), ("x_absmax", ctypes.c_float),
                 ("loglik_on_host", ctypes.c_int32), ("plan", ctypes.c_int32),
-                ("wait_limit", ctypes.c_int32), ("approx_top_k", ctypes.c_int32)]
+                ("wait_limit", ctypes.c_int32), ("approx_top_k", ctypes.c_int32),
+                ("topm_refine", ctypes.c_int32)]
 
 
 _lib = None
@@ -116,6 +118,8 @@ def gmm_default_opts(**kw) -> gmm_opts:
             v = PREC[v]
         if k == "plan" and isinstance(v, str):
             v = PLAN[v]
+        if k == "topm_refine" and isinstance(v, str):
+            v = REFINE[v]
         setattr(o, k, v)
     return o
 

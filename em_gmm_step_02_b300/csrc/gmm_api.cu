@@ -166,6 +166,8 @@ int make_plan(Plan& p, const void* X, int64_t N, int32_t D, int32_t K, int32_t c
     return fail(GMM_ERR_INVALID_ARG, "unknown precision");
   if (o.plan < GMM_PLAN_AUTO || o.plan > GMM_PLAN_SPLIT) return fail(GMM_ERR_INVALID_ARG, "unknown plan");
   if (o.wait_limit < 0) return fail(GMM_ERR_INVALID_ARG, "wait_limit must be >= 0");
+  if (o.topm_refine < GMM_REFINE_AUTO || o.topm_refine > GMM_REFINE_OFF)
+    return fail(GMM_ERR_INVALID_ARG, "topm_refine must be 0 (AUTO), 1 (ON) or 2 (OFF)");
   if (!(o.reg_covar >= 0.f) || !(o.var_floor >= 0.f) || !std::isfinite(o.reg_covar) || !std::isfinite(o.var_floor))
     return fail(GMM_ERR_INVALID_ARG, "reg_covar and var_floor must be finite and >= 0");
   if (!(o.x_absmax >= 0.f) || !std::isfinite(o.x_absmax)) return fail(GMM_ERR_INVALID_ARG, "x_absmax must be finite and >= 0");
@@ -616,17 +618,29 @@ int sync_status(uint8_t* ws, cudaStream_t s) {
   return GMM_OK;
 }
 
+// Blocks of the refinement kernel (256 threads, four points per warp): two per
+// SM, at most kRefineMaxBlocks (its log-likelihood partials).
+constexpr int kRefineMaxBlocks = 4096;
+
 // Workspace of the top-m pass placed from byte `base` on: per-group
-// candidate lists of the K > 1024 plan.
+// candidate lists of the K > 1024 plan, then (spherical and diagonal
+// covariance) the refinement's per-component rows (mu, 1/s2) padded to kMaxD
+// features, its constants (K) and its log-likelihood partials.
 struct TopmSpace {
-  size_t off_gval, off_gidx, end;
+  size_t off_gval, off_gidx, off_ivar, off_cdir, off_rll, end;
 };
 TopmSpace topm_space(const Plan& p, int m, size_t base) {
-  TopmSpace t{base, base, base};
+  TopmSpace t{base, base, base, base, base, base};
   if (p.two_pass) {
     const size_t lb = align256(sizeof(float) * static_cast<size_t>(p.n_kgroups) * p.N * m);
     t.off_gidx = base + lb;
     t.end = t.off_gidx + lb;
+  }
+  if (p.cov_diag != GMM_TIED) {
+    t.off_ivar = t.end;
+    t.off_cdir = t.off_ivar + align256(2 * sizeof(float) * static_cast<size_t>(p.K) * kMaxD);
+    t.off_rll = t.off_cdir + align256(sizeof(float) * p.K);
+    t.end = t.off_rll + align256(sizeof(double) * kRefineMaxBlocks);
   }
   return t;
 }
@@ -649,9 +663,17 @@ size_t topm_smem(const Plan& p, int m) {
 
 // The top-m pass over X: each point's m largest responsibilities and their
 // components into resp_out / idx_out (N x m, device); the total
-// log-likelihood into ll_dev when it is not NULL.
+// log-likelihood into ll_dev when it is not NULL.  When refinement is on
+// (refine_mode: gmm_refine_t; AUTO = PRECISE only) and the covariance is
+// spherical or diagonal, the pass's candidates are then refined from the
+// direct form of the log-density (topm_refine.cu: responsibilities, order
+// and log-likelihood) using the parameters as given.
 int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_out, double* ll_dev, uint8_t* ws,
-             const TopmSpace& ts, cudaStream_t s) {
+             const TopmSpace& ts, cudaStream_t s, const float* log_weights, const float* means,
+             const float* vars, int refine_mode) {
+  const bool refine = p.cov_diag != GMM_TIED && p.N > 0 &&
+                      (refine_mode == GMM_REFINE_ON || (refine_mode == GMM_REFINE_AUTO && !p.fast));
+  double* ll_pass = refine ? nullptr : ll_dev;
   const int maxm = m <= 2 ? 2 : m <= 4 ? 4 : m <= 8 ? 8 : 16;
   const int C = p.two_pass ? p.C1 : p.C;
   const bool team = topm_two_team(p, m);
@@ -671,8 +693,8 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
     a.topm_val = resp_out;
     a.topm_idx = idx_out;
     if ((r = launch_main(fn, dim3(p.C * p.tg, 1), dim3(threads), smem, s, p.C, a))) return r;
-    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
-                              static_cast<const double*>(a.ll_part), p.tg * p.C, ll_dev)))
+    if (ll_pass && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
+                               static_cast<const double*>(a.ll_part), p.tg * p.C, ll_pass)))
       return r;
   } else {
     a.C = p.C1;
@@ -685,8 +707,26 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
                     static_cast<const int32_t*>(a.topm_idx), p.n_kgroups, p.N, m, resp_out, idx_out,
                     a.ll_part)))
       return r;
-    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
-                              static_cast<const double*>(a.ll_part), kCombineBlocks, ll_dev)))
+    if (ll_pass && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1,
+                               static_cast<const double*>(a.ll_part), kCombineBlocks, ll_pass)))
+      return r;
+  }
+  if (refine) {
+    float2* pm = reinterpret_cast<float2*>(ws + ts.off_ivar);
+    float* cdir = reinterpret_cast<float*>(ws + ts.off_cdir);
+    double* rll = ll_dev ? reinterpret_cast<double*>(ws + ts.off_rll) : nullptr;
+    // 32 points per block
+    const int64_t want = (p.N + 31) / 32;
+    const int nblk = static_cast<int>(std::min<int64_t>(want, std::min(2 * device_sms(), kRefineMaxBlocks)));
+    const bool vec = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && p.D % (p.x_bf16 ? 8 : 4) == 0;
+    if ((r = launch(refine_params_handle(), dim3(p.K), dim3(kMaxD), 0, s, 1, log_weights, means, vars, p.D,
+                    p.cov_diag, pm, cdir)))
+      return r;
+    if ((r = launch(refine_handle(p.x_bf16 != 0, vec, maxm), dim3(nblk), dim3(256), 0, s, 1, X, p.N, p.D, p.K, m,
+                    reinterpret_cast<const float4*>(pm), static_cast<const float*>(cdir), resp_out, idx_out, rll)))
+      return r;
+    if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1, static_cast<const double*>(rll),
+                              nblk, ll_dev)))
       return r;
   }
   if (ll_dev && p.cov_diag == GMM_TIED) {
@@ -802,6 +842,8 @@ void gmm_default_opts(gmm_opts* o) {
   o->loglik_on_host = 0;
   o->plan = GMM_PLAN_AUTO;
   o->wait_limit = 0;
+  o->approx_top_k = 0;
+  o->topm_refine = GMM_REFINE_AUTO;
 }
 
 const char* gmm_last_error(void) { return g_error.c_str(); }
@@ -864,7 +906,7 @@ int gmm_em_step(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov_type
     if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
     double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
     if ((r = run_topm(p, X, k, reinterpret_cast<float*>(ws + t.off_r), reinterpret_cast<int32_t*>(ws + t.off_i),
-                      ll_dev, ws, t.tm, s)))
+                      ll_dev, ws, t.tm, s, log_weights, means, vars, o.topm_refine)))
       return r;
     if ((r = run_topk_mstep(p, X, k, o, ws, t, means, vars, new_log_weights, new_means, new_vars, s))) return r;
     if (o.loglik_on_host) {
@@ -984,7 +1026,8 @@ int gmm_predict_topm(const void* X, int64_t N, int32_t D, int32_t K, int32_t cov
   if ((r = set_smem_attr(topm_fn(p, m), topm_smem(p, m)))) return r;
   if ((r = run_prep(p, X, log_weights, means, vars, o, ws, s))) return r;
   double* ll_dev = o.loglik_on_host ? reinterpret_cast<double*>(ws + p.off_ll) : total_loglik;
-  if ((r = run_topm(p, X, m, resp_out, idx_out, ll_dev, ws, ts, s))) return r;
+  if ((r = run_topm(p, X, m, resp_out, idx_out, ll_dev, ws, ts, s, log_weights, means, vars, o.topm_refine)))
+    return r;
   if (o.loglik_on_host) {
     CUDA_TRY(cudaMemcpyAsync(total_loglik, ll_dev, sizeof(double), cudaMemcpyDeviceToHost, s));
     return sync_status(ws, s);
@@ -1030,7 +1073,7 @@ int gmm_assign_threshold(const void* X, int64_t N, int32_t D, int32_t K, int32_t
   float* tr = reinterpret_cast<float*>(ws + off_r);
   int32_t* ti = reinterpret_cast<int32_t*>(ws + off_i);
   int64_t* bt = reinterpret_cast<int64_t*>(ws + off_b);
-  if ((r = run_topm(p, X, m, tr, ti, nullptr, ws, ts, s))) return r;
+  if ((r = run_topm(p, X, m, tr, ti, nullptr, ws, ts, s, log_weights, means, vars, o.topm_refine))) return r;
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   if ((r = launch(kernel_handle(K_THRESH_COUNT), dim3(static_cast<unsigned>(n_blocks)), dim3(kThreshBlock), 0, s, 1,
                   static_cast<const float*>(tr), N, m, tau, offsets, bt)))

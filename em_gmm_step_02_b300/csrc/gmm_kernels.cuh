@@ -74,6 +74,12 @@ constexpr int kTkChunk = 2048;
 enum TopkKernel : int { TK_COUNT, TK_SCAN, TK_BASE, TK_FILL, TK_STATS, TK_STATS_VEC, TK_FINAL };
 const void* topk_handle(TopkKernel id, bool xb);
 
+// topm_refine.cu: direct-form recomputation of the top-m candidates' logits
+// (per-component rows (mu, 1/s2) padded to kMaxD features and constants, then
+// eight lanes per point; vec: 16-byte loads of X; maxm 2/4/8/16).
+const void* refine_params_handle();
+const void* refine_handle(bool xb, bool vec, int maxm);
+
 // Host-side handle of a kernel, for cudaLaunchKernelEx (argument order and
 // types as in gmm_kernels.cu).
 const void* kernel_handle(KernelId id);

@@ -1,0 +1,243 @@
+// topm_refine.cu -- the top-m responsibilities recomputed from the direct form
+// of the Gaussian log-density ("Flash-GMM: A Memory-Efficient Kernel for
+// Scalable Soft Clustering", section 2: log pi_k + log N(x | mu_k, Sigma_k)
+// with the squared distance (x - mu)^2 / s2, not its expansion).
+//
+// The top-m pass ranks components by logits from the tensor cores, where the
+// expanded form [x, x^2] . [mu / s2, -1 / (2 s2)] carries a rounding error
+// that grows with x^2 / s2 (sharply fitted components).  Its candidates are
+// kept; their logits are recomputed here in fp32 from x, mu and s2:
+//   l'_k = c_k - 1/2 sum_d (x_d - mu_kd)^2 / s2_kd,
+//   c_k  = log pi_k - 1/2 sum_d log(2 pi s2_kd),
+// and the mass the pass gave the candidates, R = sum_j r_j (all K
+// normalised), is redistributed among them by the recomputed logits:
+//   r'_j = R exp(l'_j) / sum_i exp(l'_i),
+// then the list is sorted again (descending, equal values by the lower
+// component).  R itself is the pass's; at fitted parameters it is 1 up to
+// the non-candidates' share.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "gmm_kernels.cuh"
+
+namespace gmm {
+
+namespace {
+
+// Per-component rows of the refinement, padded to kMaxD features:
+// pm[k][d] = (mu_kd, 1 / s2_kd) for d < D (spherical: s2_k for every d) and
+// (0, 0) beyond, so that padding adds nothing to the distance; cdir[k] = c_k
+// (-inf for a dead component, log pi_k = -inf).  One block of kMaxD threads
+// per component.
+__global__ void __launch_bounds__(kMaxD) refine_params_kernel(const float* __restrict__ log_weights,
+                                                              const float* __restrict__ means,
+                                                              const float* __restrict__ vars, int D, int cov_diag,
+                                                              float2* __restrict__ pm, float* __restrict__ cdir) {
+  __shared__ double red[kMaxD];
+  const int k = blockIdx.x, d = threadIdx.x;
+  double lg = 0.0;
+  float2 e = make_float2(0.f, 0.f);
+  if (d < D) {
+    const int64_t o = static_cast<int64_t>(k) * D + d;
+    const double v = cov_diag ? vars[o] : vars[k];
+    e = make_float2(means[o], static_cast<float>(1.0 / v));
+    lg = log(2.0 * 3.14159265358979323846 * v);
+  }
+  pm[static_cast<int64_t>(k) * kMaxD + d] = e;
+  red[d] = lg;
+  __syncthreads();
+  if (d == 0) {
+    double s = 0.0;
+    for (int i = 0; i < D; ++i) s += red[i];
+    const float lw = log_weights[k];
+    cdir[k] = lw == -INFINITY ? -INFINITY : static_cast<float>(static_cast<double>(lw) - 0.5 * s);
+  }
+}
+
+// Features [16 q, 16 q + 16) of row n into v (0 past D).  VEC: 16-byte loads
+// (the row starts on a 16-byte boundary and D is a multiple of 8 for bf16, of
+// 4 for float32).
+template <bool XB, bool VEC>
+__device__ __forceinline__ void load_x16(const void* X, int64_t n, int D, int q, float (&v)[16]) {
+  const int d0 = 16 * q;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = 0.f;
+  if (d0 >= D) return;
+  if constexpr (VEC && XB) {
+    const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(X) + n * D + d0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (d0 + 8 * h < D) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + 8 * h));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * h + 2 * i] = __uint_as_float(w[i] << 16);
+          v[8 * h + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+      }
+    }
+  } else if constexpr (VEC) {
+    const float* row = reinterpret_cast<const float*>(X) + n * D + d0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      if (d0 + 4 * h < D) {
+        const float4 u = __ldg(reinterpret_cast<const float4*>(row + 4 * h));
+        v[4 * h] = u.x;
+        v[4 * h + 1] = u.y;
+        v[4 * h + 2] = u.z;
+        v[4 * h + 3] = u.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (d0 + i < D) {
+        if constexpr (XB) v[i] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(X)[n * D + d0 + i]);
+        else v[i] = reinterpret_cast<const float*>(X)[n * D + d0 + i];
+      }
+    }
+  }
+}
+
+// Eight lanes per point (lane q of the group holds features [16 q, 16 q + 16)),
+// four points per warp; the next point's candidate list is loaded while the
+// current one is refined.  Every lane of a group ends with the whole sorted
+// list; lane q writes entries q and q + 8.  With ll_part set, each block
+// writes the sum over its points of  log sum_j exp(l'_j) - log R  (the
+// point's log-likelihood: the candidates carry the share R of the density).
+template <bool XB, bool VEC, int MAXM>
+__global__ void __launch_bounds__(256, 2) refine_kernel(const void* __restrict__ X, int64_t N, int D, int K, int m,
+                                                        const float4* __restrict__ pm,
+                                                        const float* __restrict__ cdir, float* __restrict__ resp,
+                                                        int32_t* __restrict__ idx, double* __restrict__ ll_part) {
+  __shared__ double red[8];
+  const int lane = threadIdx.x & 31, g = lane >> 3, q = lane & 7;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5) * 4;
+  int64_t n = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 4 + g;
+  const bool lanes_used = 16 * q < D;
+  int32_t cn[MAXM];
+#pragma unroll
+  for (int j = 0; j < MAXM; ++j) cn[j] = (j < m && n < N) ? idx[n * m + j] : -1;
+  double acc = 0.0;
+  for (; n - g < N; n += stride) {
+    const bool valid = n < N;
+    int32_t c[MAXM];
+#pragma unroll
+    for (int j = 0; j < MAXM; ++j) c[j] = cn[j];
+    const int64_t nn = n + stride;
+#pragma unroll
+    for (int j = 0; j < MAXM; ++j) cn[j] = (j < m && nn < N) ? idx[nn * m + j] : -1;
+    float x[16];
+    if (valid) load_x16<XB, VEC>(X, n, D, q, x);
+    else
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = 0.f;
+    float l[MAXM];
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < MAXM; ++j) {
+      const int k = c[j];
+      const bool live = j < m && k >= 0 && k < K;
+      const float ck = live ? __ldg(cdir + k) : -INFINITY;
+      float s = 0.f;
+      if (live && lanes_used) {
+        const float4* row = pm + (static_cast<int64_t>(k) * kMaxD + 16 * q) / 2;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float4 e = __ldg(row + h);   // (mu, 1/s2) of features 2h, 2h + 1
+          const float y0 = x[2 * h] - e.x, y1 = x[2 * h + 1] - e.z;
+          s = fmaf(y0 * y0, e.y, s);
+          s = fmaf(y1 * y1, e.w, s);
+        }
+      }
+      s += __shfl_xor_sync(0xffffffffu, s, 4);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      l[j] = ck > -INFINITY ? ck - 0.5f * s : -INFINITY;
+      lmax = fmaxf(lmax, l[j]);
+    }
+    if (!valid) continue;
+    float r[MAXM];
+    float mass = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXM; ++j) {
+      r[j] = j < m ? resp[n * m + j] : 0.f;
+      mass += r[j];
+    }
+    if (!(lmax > -INFINITY && mass > 0.f)) {
+      if (q == 0) acc += -INFINITY;
+      continue;
+    }
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXM; ++j) {
+      l[j] = l[j] > -INFINITY ? expf(l[j] - lmax) : 0.f;
+      z += l[j];
+    }
+    const float f = mass / z;
+#pragma unroll
+    for (int j = 0; j < MAXM; ++j) r[j] = j < m ? l[j] * f : -INFINITY;
+    if (q == 0) acc += static_cast<double>(lmax) + static_cast<double>(logf(z)) - static_cast<double>(logf(mass));
+    // descending r, equal values by the lower component (bubble passes over
+    // compile-time positions keep the lists in registers; entries past m
+    // hold -inf and stay last)
+#pragma unroll
+    for (int a = 0; a < MAXM - 1; ++a) {
+#pragma unroll
+      for (int b = 0; b < MAXM - 1 - a; ++b) {
+        const bool sw = r[b] < r[b + 1] || (r[b] == r[b + 1] && c[b] > c[b + 1]);
+        const float tr = sw ? r[b + 1] : r[b];
+        const float ur = sw ? r[b] : r[b + 1];
+        const int32_t tc = sw ? c[b + 1] : c[b];
+        const int32_t uc = sw ? c[b] : c[b + 1];
+        r[b] = tr;
+        r[b + 1] = ur;
+        c[b] = tc;
+        c[b + 1] = uc;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXM; ++j) {
+      if (j < m && (j & 7) == q) {
+        resp[n * m + j] = r[j];
+        idx[n * m + j] = c[j];
+      }
+    }
+  }
+  if (ll_part) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double t = 0.0;
+      for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += red[i];
+      ll_part[blockIdx.x] = t;
+    }
+  }
+}
+
+template <bool XB, bool VEC>
+const void* refine_fn(int maxm) {
+  switch (maxm) {
+    case 2: return reinterpret_cast<const void*>(&refine_kernel<XB, VEC, 2>);
+    case 4: return reinterpret_cast<const void*>(&refine_kernel<XB, VEC, 4>);
+    case 8: return reinterpret_cast<const void*>(&refine_kernel<XB, VEC, 8>);
+    case 16: return reinterpret_cast<const void*>(&refine_kernel<XB, VEC, 16>);
+  }
+  return nullptr;
+}
+
+}  // namespace
+
+const void* refine_params_handle() { return reinterpret_cast<const void*>(&refine_params_kernel); }
+
+const void* refine_handle(bool xb, bool vec, int maxm) {
+  return xb ? (vec ? refine_fn<true, true>(maxm) : refine_fn<true, false>(maxm))
+            : (vec ? refine_fn<false, true>(maxm) : refine_fn<false, false>(maxm));
+}
+
+}  // namespace gmm

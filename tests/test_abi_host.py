@@ -24,6 +24,21 @@ def test_default_opts():
     o = G.gmm_default_opts()
     assert o.precision == 0 and o.loglik_on_host == 0
     assert abs(o.reg_covar - 1e-6) < 1e-12 and o.var_floor == 0.0 and o.x_absmax == 0.0
+    assert o.approx_top_k == 0 and o.topm_refine == 0 and o.plan == 0 and o.wait_limit == 0
+    # every field is written, whatever the struct held before
+    junk = G.gmm_opts(precision=7, approx_top_k=9, topm_refine=5, wait_limit=3, plan=4)
+    G.lib().gmm_default_opts(ctypes.byref(junk))
+    assert (junk.precision, junk.approx_top_k, junk.topm_refine, junk.wait_limit, junk.plan) == (0, 0, 0, 0, 0)
+
+
+@pytest.mark.parametrize("v", [-1, 3])
+def test_topm_refine_argument_error(v):
+    assert _call(opts=G.gmm_default_opts(topm_refine=v)) == -1
+    assert "topm_refine" in G.gmm_last_error()
+    # a valid setting passes this check (the call may still fail later, e.g.
+    # for want of a device)
+    _call(opts=G.gmm_default_opts(topm_refine="on"))
+    assert "topm_refine" not in G.gmm_last_error()
 
 
 def _call(N=100, D=8, K=4, cov=1, dt=0, X=0x1000, p=0x2000, ll=0x3000, opts=None):

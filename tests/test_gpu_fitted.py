@@ -36,7 +36,25 @@ expanded-form terms (22-bit operand pieces, fp32 accumulation).  At the fitted
 spherical parameters (regulariser 1e-3 of the data variance) max_i T_i r_i
 (1 - r_i) over the points' best components is about 1.3e3 log2 units, an error
 of 2^-22 * 1.3e3 * ln 2 = 2.2e-4 (measured: 3e-4).  Each entry is therefore
-held to the larger of 1e-4 and that bound (gpu_util.precise_resp_tol)."""
+held to the larger of 1e-4 and that bound (gpu_util.precise_resp_tol); the
+per-point log-likelihood of PRECISE likewise to the larger of 1e-4 and the
+mean of the rows' logit resolution (a row's log-sum-exp moves by at most its
+largest logit error).  On the float32 descriptor workload (integers up to
+255, fitted standard deviations of a few units) the expanded form's terms
+reach ~1e4 log2 units per point: its fitted log-likelihood is off by 7.9e-4
+per point against a bound of ~8e-3, while weights, means and variances stay
+within 1e-4.
+
+Sharp large-K fit (24576 rows, K = 8192, regulariser 1e-3 of the data
+variance: about three points per component).  The top-m pass is compared for
+PRECISE (refined by default) and for FAST with the refinement switched on:
+the candidates' responsibilities and the log-likelihood come from the
+direct-form refinement (topm_refine.cu) and agree to ~1e-5.  FAST without it
+is off by up to 6e-2 there (fp16 rounding of the expanded form).  The EM step
+is not compared there: the M-step of components holding a few points follows
+the expanded-form logits, whose resolution (above) moves their weights by
+~4e-3 and means by ~4e-2 of sigma on PRECISE (log-likelihood within the
+derived bound)."""
 import numpy as np
 import pytest
 import torch
@@ -75,6 +93,16 @@ CASES = [
     ("spherical_1m", 20000, 10, "precise", 3, 0.0, False),
     ("spherical_1m", 20000, 10, "precise", 3, 1e-3, True),
     ("largek_2m", 8192, 4, "fast", 8, 0.0, False),
+    ("descriptor_100m", 20000, 5, "precise", 4, 1e-3, True),   # float32, D = 128: streamed parameters
+]
+
+# top-m passes compared: the cases above with the log-likelihood compared, the
+# collapsed large-K fit, and both paths at a sharp large-K fit (regulariser in
+# data units, about three points per component), where the candidates'
+# responsibilities and the log-likelihood come from the direct-form refinement
+TOPM_CASES = [c + ("auto",) for c in CASES if c[6] or c[0] == "largek_2m"] + [
+    ("largek_2m", 24576, 3, "precise", 8, 1e-3, True, "auto"),
+    ("largek_2m", 24576, 3, "fast", 8, 1e-3, True, "on"),
 ]
 
 
@@ -92,6 +120,12 @@ def test_em_step_at_fitted_parameters(name, rows, iters, path, m, rel_reg, full)
     e_w, e_mu, e_v, msg = elementwise_errors(got, ref, X.shape[0], w.cov, path, tol, w.x_dtype, mu)
     e_ll = abs(float(out[3].item()) - ref[3]) / X.shape[0]
     msg += f" ll/N {e_ll:.2e}"
+    if full and path == "precise":
+        # the log-likelihood's bound from the logit resolution of PRECISE
+        # (gpu_util.precise_resp_tol), over each point's best components
+        r_o, i_o, _ = oracle.topm(X.float().numpy(), lw, mu, var, w.cov, m)
+        tol_ll = precise_resp_tol(X.float().numpy(), mu, var, w.cov, i_o, r_o, tol, tol_ll)[1]
+        msg += f" (bound {tol_ll:.2e})"
     print(msg)
     assert e_w <= 1 and e_mu <= 1 and e_v <= 1, msg
     if full:
@@ -99,12 +133,12 @@ def test_em_step_at_fitted_parameters(name, rows, iters, path, m, rel_reg, full)
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,rows,iters,path,m,rel_reg,full", [c for c in CASES if c[6] or c[0] == "largek_2m"])
-def test_topm_at_fitted_parameters(name, rows, iters, path, m, rel_reg, full):
+@pytest.mark.parametrize("name,rows,iters,path,m,rel_reg,full,refine", TOPM_CASES)
+def test_topm_at_fitted_parameters(name, rows, iters, path, m, rel_reg, full, refine):
     w, X, (lw, mu, var), reg = fitted(name, rows, iters, rel_reg)
     tol, tol_ll = TOL[path]
     p = params_to_device(lw, mu, var)
-    r, idx, ll = G.gmm_predict_topm(X.cuda(), *p, w.cov, m, precision=path)
+    r, idx, ll = G.gmm_predict_topm(X.cuda(), *p, w.cov, m, precision=path, topm_refine=refine)
     torch.cuda.synchronize()
     assert G.gmm_stream_status() == 0, G.gmm_last_error()
     r_o, i_o, ll_o = oracle.topm(X.float().numpy(), lw, mu, var, w.cov, min(m + 1, w.K))

@@ -71,11 +71,11 @@ def sharpened(X_cpu, init, cov, iters):
     return tuple(np.asarray(a, np.float32) for a in (lw, mu, var))
 
 
-def run_case(X_cpu, lw, mu, var, cov, m, precision="auto"):
+def run_case(X_cpu, lw, mu, var, cov, m, precision="auto", refine="auto"):
     K = len(lw)
     X = X_cpu.cuda()
     p = params_to_device(lw, mu, var)
-    r, idx, ll = G.gmm_predict_topm(X, *p, cov, m, precision=precision)
+    r, idx, ll = G.gmm_predict_topm(X, *p, cov, m, precision=precision, topm_refine=refine)
     torch.cuda.synchronize()
     assert G.gmm_stream_status() == 0, G.gmm_last_error()
     mo = min(m + 1, K)
@@ -118,6 +118,25 @@ def test_topm_small(N, D, K, cov, xd, m):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("N,D,K,cov,xd,m", [CASES[i] for i in (0, 1, 2, 3, 5, 6, 10, 11)])
+def test_topm_refinement_switched(N, D, K, cov, xd, m):
+    """The other setting of the direct-form refinement than the path's
+    default: FAST with it on, PRECISE with it off; each within its path's
+    bound (the refinement keeps the pass's candidates and their share)."""
+    w = W.generic(N, D, K, cov, xd, seed=N + 3 * D + K)
+    X = W.make_data(w)
+    init = W.make_init(w, X)
+    path = "fast" if xd == "bf16" else "precise"
+    lw, mu, var = init if path == "fast" else sharpened(X, init, cov, 2)
+    out = run_case(X, lw, mu, var, cov, m, refine="on" if path == "fast" else "off")
+    tol, tol_ll = TOL[path]
+    if path == "precise":
+        tol, tol_ll = precise_resp_tol(X.float().numpy(), mu, var, cov, out[4][:, :m], out[3][:, :m], tol, tol_ll)
+    err, n_sure = check_topm(*out[:3], *out[3:], N, m, tol, tol_ll)
+    print(f"max |dr| {err:.2e}, {n_sure} separated entries checked")
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("name,rows,m", [("tiny_diag", 4096, 2), ("embed_10m", 20000, 4),
                                           ("largek_2m", 30000, 8)])
 def test_topm_workload_prefix(name, rows, m):
@@ -151,14 +170,16 @@ def test_topm_dead_components_and_m1():
 
 
 @pytest.mark.gpu
-def test_topm_full_size_embed_sampled_rows():
-    """The full 10M x 128 x 1024 workload in one launch; rows are independent,
-    so a sample of rows is checked against the oracle run on those rows alone."""
+@pytest.mark.parametrize("refine", ["auto", "on"])
+def test_topm_full_size_embed_sampled_rows(refine):
+    """The full 10M x 128 x 1024 workload in one launch (FAST; with and
+    without the refinement); rows are independent, so a sample of rows is
+    checked against the oracle run on those rows alone."""
     w = W.WORKLOADS["embed_10m"]
     X = W.make_data(w, device="cuda")
     lw, mu, var = W.make_init(w, X)
     p = params_to_device(lw, mu, var)
-    r, idx, ll = G.gmm_predict_topm(X, *p, w.cov, 4)
+    r, idx, ll = G.gmm_predict_topm(X, *p, w.cov, 4, topm_refine=refine)
     torch.cuda.synchronize()
     assert G.gmm_stream_status() == 0
     rng = np.random.default_rng(0)
