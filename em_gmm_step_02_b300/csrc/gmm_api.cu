@@ -618,8 +618,8 @@ int sync_status(uint8_t* ws, cudaStream_t s) {
   return GMM_OK;
 }
 
-// Blocks of the refinement kernel (256 threads, four points per warp): two per
-// SM, at most kRefineMaxBlocks (its log-likelihood partials).
+// Blocks of the refinement kernel (256 threads, four points per warp): as many
+// as are resident at once, at most kRefineMaxBlocks (its log-likelihood partials).
 constexpr int kRefineMaxBlocks = 4096;
 
 // Workspace of the top-m pass placed from byte `base` on: per-group
@@ -715,14 +715,18 @@ int run_topm(const Plan& p, const void* X, int m, float* resp_out, int32_t* idx_
     float2* pm = reinterpret_cast<float2*>(ws + ts.off_ivar);
     float* cdir = reinterpret_cast<float*>(ws + ts.off_cdir);
     double* rll = ll_dev ? reinterpret_cast<double*>(ws + ts.off_rll) : nullptr;
-    // 32 points per block
+    // 32 points per block; as many blocks as are resident at once
+    const bool vec = p.D % 2 == 0 && (reinterpret_cast<uintptr_t>(X) & (p.x_bf16 ? 3 : 7)) == 0;
+    const void* rfn = refine_handle(p.x_bf16 != 0, vec, maxm);
+    int per_sm = 2;
+    CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rfn, 256, 0));
     const int64_t want = (p.N + 31) / 32;
-    const int nblk = static_cast<int>(std::min<int64_t>(want, std::min(2 * device_sms(), kRefineMaxBlocks)));
-    const bool vec = (reinterpret_cast<uintptr_t>(X) & 15) == 0 && p.D % (p.x_bf16 ? 8 : 4) == 0;
+    const int nblk = static_cast<int>(
+        std::min<int64_t>(want, std::min(std::max(per_sm, 1) * device_sms(), kRefineMaxBlocks)));
     if ((r = launch(refine_params_handle(), dim3(p.K), dim3(kMaxD), 0, s, 1, log_weights, means, vars, p.D,
                     p.cov_diag, pm, cdir)))
       return r;
-    if ((r = launch(refine_handle(p.x_bf16 != 0, vec, maxm), dim3(nblk), dim3(256), 0, s, 1, X, p.N, p.D, p.K, m,
+    if ((r = launch(rfn, dim3(nblk), dim3(256), 0, s, 1, X, p.N, p.D, p.K, m,
                     reinterpret_cast<const float4*>(pm), static_cast<const float*>(cdir), resp_out, idx_out, rll)))
       return r;
     if (ll_dev && (r = launch(kernel_handle(K_LL_TOTAL), dim3(1), dim3(32), 0, s, 1, static_cast<const double*>(rll),

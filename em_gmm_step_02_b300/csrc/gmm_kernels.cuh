@@ -76,7 +76,7 @@ const void* topk_handle(TopkKernel id, bool xb);
 
 // topm_refine.cu: direct-form recomputation of the top-m candidates' logits
 // (per-component rows (mu, 1/s2) padded to kMaxD features and constants, then
-// eight lanes per point; vec: 16-byte loads of X; maxm 2/4/8/16).
+// eight lanes per point; vec: X read as feature pairs; maxm 2/4/8/16).
 const void* refine_params_handle();
 const void* refine_handle(bool xb, bool vec, int maxm);
 

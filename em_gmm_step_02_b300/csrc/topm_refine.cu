@@ -56,60 +56,53 @@ __global__ void __launch_bounds__(kMaxD) refine_params_kernel(const float* __res
   }
 }
 
-// Features [16 q, 16 q + 16) of row n into v (0 past D).  VEC: 16-byte loads
-// (the row starts on a 16-byte boundary and D is a multiple of 8 for bf16, of
-// 4 for float32).
+// Features 16 h + 2 q and 16 h + 2 q + 1 (h = 0..7) of row n into v[2 h],
+// v[2 h + 1] (0 past D): the eight lanes of a group read 32 (bf16) or 64
+// (float32) contiguous bytes per load.  VEC: one 4- or 8-byte load per pair
+// (D even, X aligned to the pair).
 template <bool XB, bool VEC>
 __device__ __forceinline__ void load_x16(const void* X, int64_t n, int D, int q, float (&v)[16]) {
-  const int d0 = 16 * q;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = 0.f;
-  if (d0 >= D) return;
-  if constexpr (VEC && XB) {
-    const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(X) + n * D + d0;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (d0 + 8 * h < D) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + 8 * h));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[8 * h + 2 * i] = __uint_as_float(w[i] << 16);
-          v[8 * h + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
+  for (int h = 0; h < 8; ++h) {
+    const int d = 16 * h + 2 * q;
+    float v0 = 0.f, v1 = 0.f;
+    if constexpr (VEC && XB) {
+      if (d < D) {
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(X) + n * D + d));
+        v0 = __uint_as_float(w << 16);
+        v1 = __uint_as_float(w & 0xffff0000u);
+      }
+    } else if constexpr (VEC) {
+      if (d < D) {
+        const float2 u = __ldg(reinterpret_cast<const float2*>(reinterpret_cast<const float*>(X) + n * D + d));
+        v0 = u.x;
+        v1 = u.y;
+      }
+    } else {
+      if constexpr (XB) {
+        const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(X) + n * D;
+        if (d < D) v0 = __bfloat162float(row[d]);
+        if (d + 1 < D) v1 = __bfloat162float(row[d + 1]);
+      } else {
+        const float* row = reinterpret_cast<const float*>(X) + n * D;
+        if (d < D) v0 = row[d];
+        if (d + 1 < D) v1 = row[d + 1];
       }
     }
-  } else if constexpr (VEC) {
-    const float* row = reinterpret_cast<const float*>(X) + n * D + d0;
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      if (d0 + 4 * h < D) {
-        const float4 u = __ldg(reinterpret_cast<const float4*>(row + 4 * h));
-        v[4 * h] = u.x;
-        v[4 * h + 1] = u.y;
-        v[4 * h + 2] = u.z;
-        v[4 * h + 3] = u.w;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (d0 + i < D) {
-        if constexpr (XB) v[i] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(X)[n * D + d0 + i]);
-        else v[i] = reinterpret_cast<const float*>(X)[n * D + d0 + i];
-      }
-    }
+    v[2 * h] = v0;
+    v[2 * h + 1] = v1;
   }
 }
 
-// Eight lanes per point (lane q of the group holds features [16 q, 16 q + 16)),
-// four points per warp; the next point's candidate list is loaded while the
+// Eight lanes per point (lane q of the group holds the feature pairs 8 h + q,
+// h = 0..7, so that the group reads one 128-byte line of a candidate's row
+// per load), four points per warp; the next point's candidate list is loaded while the
 // current one is refined.  Every lane of a group ends with the whole sorted
 // list; lane q writes entries q and q + 8.  With ll_part set, each block
 // writes the sum over its points of  log sum_j exp(l'_j) - log R  (the
 // point's log-likelihood: the candidates carry the share R of the density).
 template <bool XB, bool VEC, int MAXM>
-__global__ void __launch_bounds__(256, 2) refine_kernel(const void* __restrict__ X, int64_t N, int D, int K, int m,
+__global__ void __launch_bounds__(256, 3) refine_kernel(const void* __restrict__ X, int64_t N, int D, int K, int m,
                                                         const float4* __restrict__ pm,
                                                         const float* __restrict__ cdir, float* __restrict__ resp,
                                                         int32_t* __restrict__ idx, double* __restrict__ ll_part) {
@@ -117,7 +110,6 @@ __global__ void __launch_bounds__(256, 2) refine_kernel(const void* __restrict__
   const int lane = threadIdx.x & 31, g = lane >> 3, q = lane & 7;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5) * 4;
   int64_t n = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 4 + g;
-  const bool lanes_used = 16 * q < D;
   int32_t cn[MAXM];
 #pragma unroll
   for (int j = 0; j < MAXM; ++j) cn[j] = (j < m && n < N) ? idx[n * m + j] : -1;
@@ -143,14 +135,16 @@ __global__ void __launch_bounds__(256, 2) refine_kernel(const void* __restrict__
       const bool live = j < m && k >= 0 && k < K;
       const float ck = live ? __ldg(cdir + k) : -INFINITY;
       float s = 0.f;
-      if (live && lanes_used) {
-        const float4* row = pm + (static_cast<int64_t>(k) * kMaxD + 16 * q) / 2;
+      if (live) {
+        const float4* row = pm + static_cast<int64_t>(k) * (kMaxD / 2) + q;
 #pragma unroll
         for (int h = 0; h < 8; ++h) {
-          const float4 e = __ldg(row + h);   // (mu, 1/s2) of features 2h, 2h + 1
-          const float y0 = x[2 * h] - e.x, y1 = x[2 * h + 1] - e.z;
-          s = fmaf(y0 * y0, e.y, s);
-          s = fmaf(y1 * y1, e.w, s);
+          if (16 * h < D) {
+            const float4 e = __ldg(row + 8 * h);   // (mu, 1/s2) of features 16 h + 2 q, 16 h + 2 q + 1
+            const float y0 = x[2 * h] - e.x, y1 = x[2 * h + 1] - e.z;
+            s = fmaf(y0 * y0, e.y, s);
+            s = fmaf(y1 * y1, e.w, s);
+          }
         }
       }
       s += __shfl_xor_sync(0xffffffffu, s, 4);
