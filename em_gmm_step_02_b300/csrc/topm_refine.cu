@@ -56,53 +56,66 @@ __global__ void __launch_bounds__(kMaxD) refine_params_kernel(const float* __res
   }
 }
 
-// Features 16 h + 2 q and 16 h + 2 q + 1 (h = 0..7) of row n into v[2 h],
-// v[2 h + 1] (0 past D): the eight lanes of a group read 32 (bf16) or 64
-// (float32) contiguous bytes per load.  VEC: one 4- or 8-byte load per pair
-// (D even, X aligned to the pair).
+// Features 16 h + 2 q and 16 h + 2 q + 1 (h = 0..7) of row n (0 past D or
+// for n >= N), fetched into w and turned into floats by decode_x16 when they
+// are used, so that the loads of the next point stay in flight meanwhile: the
+// eight lanes of a group read 32 (bf16) or 64 (float32) contiguous bytes per
+// load.  VEC: one 4- or 8-byte load per pair (D even, X aligned to the pair;
+// bf16 pairs stay packed in w[2 h]); otherwise element loads, as float bits.
 template <bool XB, bool VEC>
-__device__ __forceinline__ void load_x16(const void* X, int64_t n, int D, int q, float (&v)[16]) {
+__device__ __forceinline__ void fetch_x16(const void* X, int64_t n, int64_t N, int D, int q, uint32_t (&w)[16]) {
 #pragma unroll
   for (int h = 0; h < 8; ++h) {
     const int d = 16 * h + 2 * q;
-    float v0 = 0.f, v1 = 0.f;
-    if constexpr (VEC && XB) {
-      if (d < D) {
-        const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(X) + n * D + d));
-        v0 = __uint_as_float(w << 16);
-        v1 = __uint_as_float(w & 0xffff0000u);
-      }
-    } else if constexpr (VEC) {
-      if (d < D) {
-        const float2 u = __ldg(reinterpret_cast<const float2*>(reinterpret_cast<const float*>(X) + n * D + d));
-        v0 = u.x;
-        v1 = u.y;
-      }
-    } else {
-      if constexpr (XB) {
+    uint32_t w0 = 0, w1 = 0;
+    if (n < N) {
+      if constexpr (VEC && XB) {
+        if (d < D)
+          w0 = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const __nv_bfloat16*>(X) + n * D + d));
+      } else if constexpr (VEC) {
+        if (d < D) {
+          const float2 u = __ldg(reinterpret_cast<const float2*>(reinterpret_cast<const float*>(X) + n * D + d));
+          w0 = __float_as_uint(u.x);
+          w1 = __float_as_uint(u.y);
+        }
+      } else if constexpr (XB) {
         const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(X) + n * D;
-        if (d < D) v0 = __bfloat162float(row[d]);
-        if (d + 1 < D) v1 = __bfloat162float(row[d + 1]);
+        if (d < D) w0 = __float_as_uint(__bfloat162float(row[d]));
+        if (d + 1 < D) w1 = __float_as_uint(__bfloat162float(row[d + 1]));
       } else {
         const float* row = reinterpret_cast<const float*>(X) + n * D;
-        if (d < D) v0 = row[d];
-        if (d + 1 < D) v1 = row[d + 1];
+        if (d < D) w0 = __float_as_uint(row[d]);
+        if (d + 1 < D) w1 = __float_as_uint(row[d + 1]);
       }
     }
-    v[2 * h] = v0;
-    v[2 * h + 1] = v1;
+    w[2 * h] = w0;
+    w[2 * h + 1] = w1;
+  }
+}
+
+template <bool XB, bool VEC>
+__device__ __forceinline__ void decode_x16(const uint32_t (&w)[16], float (&v)[16]) {
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    if constexpr (VEC && XB) {
+      v[2 * h] = __uint_as_float(w[2 * h] << 16);
+      v[2 * h + 1] = __uint_as_float(w[2 * h] & 0xffff0000u);
+    } else {
+      v[2 * h] = __uint_as_float(w[2 * h]);
+      v[2 * h + 1] = __uint_as_float(w[2 * h + 1]);
+    }
   }
 }
 
 // Eight lanes per point (lane q of the group holds the feature pairs 8 h + q,
 // h = 0..7, so that the group reads one 128-byte line of a candidate's row
-// per load), four points per warp; the next point's candidate list is loaded while the
-// current one is refined.  Every lane of a group ends with the whole sorted
+// per load), four points per warp; the next point's candidate list, row of X
+// and responsibilities are loaded while the current one is refined.  Every lane of a group ends with the whole sorted
 // list; lane q writes entries q and q + 8.  With ll_part set, each block
 // writes the sum over its points of  log sum_j exp(l'_j) - log R  (the
 // point's log-likelihood: the candidates carry the share R of the density).
 template <bool XB, bool VEC, int MAXM>
-__global__ void __launch_bounds__(256, 3) refine_kernel(const void* __restrict__ X, int64_t N, int D, int K, int m,
+__global__ void __launch_bounds__(256, MAXM >= 8 ? 2 : 3) refine_kernel(const void* __restrict__ X, int64_t N, int D, int K, int m,
                                                         const float4* __restrict__ pm,
                                                         const float* __restrict__ cdir, float* __restrict__ resp,
                                                         int32_t* __restrict__ idx, double* __restrict__ ll_part) {
@@ -111,22 +124,33 @@ __global__ void __launch_bounds__(256, 3) refine_kernel(const void* __restrict__
   const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5) * 4;
   int64_t n = ((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * 4 + g;
   int32_t cn[MAXM];
+  float rn[MAXM];
+  uint32_t wn[16];
 #pragma unroll
-  for (int j = 0; j < MAXM; ++j) cn[j] = (j < m && n < N) ? idx[n * m + j] : -1;
+  for (int j = 0; j < MAXM; ++j) {
+    cn[j] = (j < m && n < N) ? idx[n * m + j] : -1;
+    rn[j] = (j < m && n < N) ? resp[n * m + j] : 0.f;
+  }
+  fetch_x16<XB, VEC>(X, n, N, D, q, wn);
   double acc = 0.0;
   for (; n - g < N; n += stride) {
     const bool valid = n < N;
     int32_t c[MAXM];
+    float r[MAXM];
+    float x[16];
 #pragma unroll
-    for (int j = 0; j < MAXM; ++j) c[j] = cn[j];
+    for (int j = 0; j < MAXM; ++j) {
+      c[j] = cn[j];
+      r[j] = rn[j];
+    }
+    decode_x16<XB, VEC>(wn, x);
     const int64_t nn = n + stride;
 #pragma unroll
-    for (int j = 0; j < MAXM; ++j) cn[j] = (j < m && nn < N) ? idx[nn * m + j] : -1;
-    float x[16];
-    if (valid) load_x16<XB, VEC>(X, n, D, q, x);
-    else
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = 0.f;
+    for (int j = 0; j < MAXM; ++j) {
+      cn[j] = (j < m && nn < N) ? idx[nn * m + j] : -1;
+      rn[j] = (j < m && nn < N) ? resp[nn * m + j] : 0.f;
+    }
+    fetch_x16<XB, VEC>(X, nn, N, D, q, wn);
     float l[MAXM];
     float lmax = -INFINITY;
 #pragma unroll
@@ -154,13 +178,9 @@ __global__ void __launch_bounds__(256, 3) refine_kernel(const void* __restrict__
       lmax = fmaxf(lmax, l[j]);
     }
     if (!valid) continue;
-    float r[MAXM];
     float mass = 0.f;
 #pragma unroll
-    for (int j = 0; j < MAXM; ++j) {
-      r[j] = j < m ? resp[n * m + j] : 0.f;
-      mass += r[j];
-    }
+    for (int j = 0; j < MAXM; ++j) mass += r[j];
     if (!(lmax > -INFINITY && mass > 0.f)) {
       if (q == 0) acc += -INFINITY;
       continue;

@@ -126,7 +126,7 @@ typedef struct {
  * approximate top-k EM).  AUTO: on for PRECISE, off for FAST.  The
  * refinement gathers each candidate's (mu, 1/s2) row, 8 bytes per feature,
  * candidate and point (from L2), which on 10M x 128 bf16 points with m = 4
- * adds about 4 ms to a 22 ms FAST pass.  It needs a further 1 KB per
+ * adds about 2.5 ms to a 22 ms FAST pass.  It needs a further 1 KB per
  * component of workspace. */
 typedef enum { GMM_REFINE_AUTO = 0, GMM_REFINE_ON = 1, GMM_REFINE_OFF = 2 } gmm_refine_t;
 
