@@ -267,7 +267,10 @@ def gmm_em_step_noalloc(X, log_weights, means, vars_, cov="diag", *, out, opts: 
 def gmm_predict_topm(X, log_weights, means, vars_, cov="diag", m=1, *, opts: gmm_opts | None = None,
                      stream=None, **opt_kw):
     """Top-m responsibilities (N, m) float32 and indices (N, m) int32, plus the
-    total log-likelihood (1-element float64 CUDA tensor)."""
+    total log-likelihood (1-element float64 CUDA tensor).  Keywords set
+    gmm_opts fields by name, e.g. precision="fast" | "precise",
+    topm_refine="auto" | "on" | "off" (the direct-form refinement of the
+    candidates; AUTO refines PRECISE only)."""
     N, D, K, cov_i, dt = _shape(X, means, cov)
     if opts is None:
         opts = gmm_default_opts(**opt_kw)
