@@ -14,7 +14,10 @@
 //   r'_j = R exp(l'_j) / sum_i exp(l'_i),
 // then the list is sorted again (descending, equal values by the lower
 // component).  R itself is the pass's; at fitted parameters it is 1 up to
-// the non-candidates' share.
+// the non-candidates' share.  A point's log-likelihood becomes
+// log sum_j exp(l'_j) - log R.  The host runs these kernels after the pass
+// when gmm_opts.topm_refine asks for them (by default on the PRECISE path)
+// and the covariance is spherical or diagonal.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
